@@ -1,0 +1,444 @@
+#!/usr/bin/env python3
+"""Benchmark of one ragged blocked-KV attention layer forward (one step =
+rotary embedding + KV append + blocked attention over one synthetic ragged
+batch), printed as one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+value     new tokens/s per layer, inputs resident in HBM, CUDA events on the
+          launching stream, max over ranks.
+e2e       same metric through the C ABI from pinned HOST buffers: each step
+          uploads the step's qkv rows, builds + uploads the batch metadata
+          from host descriptors, runs the layer and reads the output back.
+roofline  the attention call (the dominant launches) timed live with CUDA
+          events: algorithmic bytes (or flops) per launch / mean duration.
+Multi-GPU: each rank runs its own copy of the batch (sequences are
+independent; no collective on the data path), weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from ragged_blocked_kv_raggedbatch_gb300 import workloads as W  # noqa: E402
+
+DEFAULT_WORKLOAD = "decode256_mha_d128"
+METRIC = "ragged attn new tokens/s per layer"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch of the dominant launches from an ncu capture, keyed
+# by workload, valid only while the kernel source hashes match.
+NCU_TRAFFIC = {}
+
+
+def _src_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ragged_blocked_kv_raggedbatch_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".cpp")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            hbm = d.get("hbm_gbs") or d.get("hbm_GBps") or d.get("hbm")
+            tf = d.get("bf16_tflops") or d.get("bf16_dense_tflops")
+            tfs = d.get("bf16_tflops_sustained") or tf
+            if hbm and tf:
+                return {"hbm_gbs": float(hbm), "bf16_tflops": float(tf),
+                        "bf16_tflops_sustained": float(tfs), "source": "measured"}
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def algorithmic(wl):
+    """Algorithmic work of one step (causal pairs only; bytes each read or
+    written once): dict of flops and bytes, total and per call."""
+    e = 2
+    Hq, Hkv, d = wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    s = wl.seen.astype(np.float64)
+    n = wl.new.astype(np.float64)
+    N = float(n.sum())
+    nb = wl.blocks_needed().astype(np.float64)
+    flops = 4.0 * d * Hq * float((n * s + n * (n + 1) / 2).sum())
+    step_bytes = e * (N * (Hq + 2 * Hkv) * d + N * 2 * Hkv * d + float(s.sum()) * 2 * Hkv * d
+                      + N * Hq * d) + 4 * float(nb.sum())
+    append_bytes = e * (2 * N * 2 * Hkv * d)
+    attn_bytes = e * (N * Hq * d + float((s + n).sum()) * 2 * Hkv * d + N * Hq * d) + 4 * float(nb.sum())
+    pre = wl.new > 1
+    pre_flops = 4.0 * d * Hq * float((n[pre] * s[pre] + n[pre] * (n[pre] + 1) / 2).sum())
+    return dict(flops=flops, bytes=step_bytes, append_bytes=append_bytes, attn_bytes=attn_bytes,
+                attn_flops=flops, prefill_flops=pre_flops,
+                kv_history_bytes=e * float(s.sum()) * 2 * Hkv * d)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------- CPU oracle legs
+
+def _oracle_sample(wl, n_rows_target: int, seed: int = 0, max_pool_bytes: float = 256e6):
+    """A bounded sample of the workload for the oracle: sequences drawn from
+    the batch; a prefill chunk contributes a random run of up to the remaining
+    row budget (as if it had been split there: seen += offset).  Returned as a
+    batch of its own over a compact pool (fresh values of the same
+    distribution, CPU generator), capped at ~max_pool_bytes of KV."""
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(wl.n_seqs)
+    block_bytes = 2 * wl.n_kv_heads * 64 * wl.head_dim * 2
+    seqs, rows, blocks = [], 0, 0
+    for i in order:
+        s, n = int(wl.seen[i]), int(wl.new[i])
+        take = min(n, max(1, n_rows_target - rows))
+        j0 = int(rng.integers(0, n - take + 1))
+        nb = -(-(s + j0 + take) // 64)
+        if seqs and (blocks + nb) * block_bytes > max_pool_bytes:
+            break
+        seqs.append((s + j0, take))
+        rows += take
+        blocks += nb
+        if rows >= n_rows_target:
+            break
+    return W.make_custom(seqs, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, dtype=wl.dtype,
+                         rope_theta=wl.rope_theta, value_std=wl.value_std, seed=seed,
+                         name=wl.name + "_oracle_sample")
+
+
+def time_oracle(wl, seconds: float = 12.0, seed: int = 0):
+    """Tokens/s of the oracle on the host cores over a bounded sample, re-run
+    until about `seconds` of work.  Returns (tokens/s, threads, description, s)."""
+    import oracle
+    threads = oracle.default_threads()
+    probe = _oracle_sample(wl, 1, seed + 1)
+    qkv, pool = W.make_values(probe, "cpu", seed=seed + 1)
+    t0 = time.perf_counter()
+    oracle.layer(probe, qkv, pool, n_threads=threads)
+    per_row = max(time.perf_counter() - t0, 1e-5) / probe.n_tokens
+    sub = _oracle_sample(wl, int(max(1, min(wl.n_tokens, seconds / per_row))), seed)
+    qkv, pool = W.make_values(sub, "cpu", seed=seed)
+    rows, t0 = 0, time.perf_counter()
+    while True:
+        oracle.layer(sub, qkv, pool, n_threads=threads)
+        rows += sub.n_tokens
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    desc = ("%d rows (%d sequences, %d KV-history tokens) sampled from %s, fresh values of the "
+            "same distribution, fp64 oracle meta+append+attention, repeated to %.1f s" %
+            (sub.n_tokens, sub.n_seqs, int(sub.seen.sum()), wl.name, dt))
+    return rows / dt, threads, desc, dt
+
+
+def reference_arm(args, wl):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import oracle
+    threads = oracle.default_threads()
+    # size each step so that warmup + steps take about two minutes
+    budget_s = 120.0
+    steps = args.steps + args.warmup
+    probe = _oracle_sample(wl, 1, 99)
+    qkv, pool = W.make_values(probe, "cpu", seed=99)
+    t0 = time.perf_counter()
+    oracle.layer(probe, qkv, pool, n_threads=threads)
+    per_row = max(time.perf_counter() - t0, 1e-5) / probe.n_tokens
+    rows = int(max(1, min(wl.n_tokens, budget_s / steps / per_row)))
+    samples = []
+    for k in range(min(steps, 4)):
+        sub = _oracle_sample(wl, rows, k)
+        samples.append((sub,) + tuple(W.make_values(sub, "cpu", seed=k)))
+    times, toks = [], 0
+    for k in range(steps):
+        sub, qkv, pool = samples[k % len(samples)]
+        t0 = time.perf_counter()
+        oracle.layer(sub, qkv, pool, n_threads=threads)
+        dt = time.perf_counter() - t0
+        if k >= args.warmup:
+            times.append(dt)
+            toks += sub.n_tokens
+    total = float(sum(times))
+    value = toks / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / max(1, len(times)), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "rows_per_step": samples[0][0].n_tokens},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": "about %d rows per step sampled from %s (fresh values, same "
+                                   "distribution; 4 samples reused)" % (rows, wl.name)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def gpu_arm(args, wl):
+    import torch
+    from ragged_blocked_kv_raggedbatch_gb300 import ds_ragged as R
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    dev = "cuda"
+    stream = torch.cuda.Stream()
+    peaks = load_peaks()
+    alg = algorithmic(wl)
+    nb_total = int(wl.blocks_needed().sum())
+    with torch.cuda.stream(stream):
+        qkv, pool = W.make_values(wl, dev, seed=wl.seed + rank)
+        params = R.params_for(wl)
+        layer = R.RaggedLayer(params, wl.n_seqs, wl.n_tokens, nb_total, wl.max_len(), stream=stream)
+        descs = R.SeqDescs.of(wl)
+        t0 = time.perf_counter()
+        layer.build(descs, wl.num_blocks)
+        stream.synchronize()
+        meta_build_us = 1e6 * (time.perf_counter() - t0)
+        out = torch.empty((wl.n_tokens, wl.n_q_heads * wl.head_dim), dtype=qkv.dtype, device=dev)
+    m = layer.meta
+    launches_per_step = 1 + (m.n_prefill_tiles > 0) + (m.n_decode_items > 0) + \
+        (m.n_decode_items > m.n_decode_seqs)
+
+    def step():
+        layer.append(qkv, pool)
+        layer.attention(qkv, pool, out)
+
+    flush = None
+    step_bytes = alg["bytes"]
+    if step_bytes < 2 * L2_BYTES:
+        flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    l2_note = ("inputs larger than L2 (%.2f GB per step)" % (step_bytes / 1e9) if flush is None
+               else "L2 flushed between timed steps (512 MB write, untimed)")
+
+    for _ in range(args.warmup):
+        step()
+        if flush is not None:
+            flush.zero_()
+    stream.synchronize()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            for k in range(K):
+                a, b, c = ev[k]
+                a.record(stream)
+                layer.append(qkv, pool)
+                b.record(stream)
+                layer.attention(qkv, pool, out)
+                c.record(stream)
+                if flush is not None:
+                    flush.zero_()
+        stream.synchronize()
+    clocks = clk.summary()
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    attn_ms = [b.elapsed_time(c) for a, b, c in ev]
+    app_ms = [a.elapsed_time(b) for a, b, c in ev]
+    total_ms = float(sum(step_ms))
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    torch.cuda.synchronize()
+    ms_per_step = total_ms / K
+    value = ws * wl.n_tokens * K / (total_ms / 1e3)
+
+    # roofline of the attention call (the dominant launches)
+    attn_mean_s = float(np.mean(attn_ms)) / 1e3
+    hbm_t = alg["attn_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    tc_t = alg["attn_flops"] / (peaks["bf16_tflops"] * 1e12)
+    if hbm_t >= tc_t:
+        achieved = alg["attn_bytes"] / attn_mean_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    else:
+        achieved = alg["attn_flops"] / attn_mean_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"]}
+    rec = NCU_TRAFFIC.get(wl.name)
+    roof["traffic"] = rec["bytes"] if rec and rec.get("src") == _src_hash() else None
+    roof["kernel"] = "ds_blocked_attention launches (%s)" % (
+        "decode split-K + combine" if m.n_prefill_tiles == 0 else
+        "prefill tiles" if m.n_decode_items == 0 else "prefill tiles + decode split-K + combine")
+    roof["peak_source"] = peaks["source"]
+    roof["algorithmic_bytes"] = alg["attn_bytes"]
+    roof["algorithmic_flops"] = alg["attn_flops"]
+    roof["mean_ms"] = attn_mean_s * 1e3
+
+    # whole-step roofline (slower of bytes/BW and flops/peak) as a fraction
+    t_roof = max(alg["bytes"] / (peaks["hbm_gbs"] * 1e9), alg["flops"] / (peaks["bf16_tflops"] * 1e12))
+    step_frac = t_roof / (ms_per_step / 1e3)
+
+    # ---- end to end through the C ABI from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        with torch.cuda.stream(stream):
+            qkv_host = qkv.cpu().pin_memory()
+            out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        E = max(3, min(K, 200))
+        for k in range(E + 2):
+            if k == 2:
+                stream.synchronize()
+                if pg:
+                    pg.barrier()
+                t0 = time.perf_counter()
+            with torch.cuda.stream(stream):
+                qkv.copy_(qkv_host, non_blocking=True)
+                layer.build(descs, wl.num_blocks)
+                step()
+                out_host.copy_(out, non_blocking=True)
+            stream.synchronize()  # the result is on the host before the next step
+        e2e_s = time.perf_counter() - t0
+        if pg:
+            t = torch.tensor([e2e_s], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": ws * wl.n_tokens * E / e2e_s, "unit": "tokens/s",
+               "h2d_bytes_per_step": int(qkv.numel() * qkv.element_size() + m.used_bytes),
+               "d2h_bytes_per_step": int(out.numel() * out.element_size()), "steps": E}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, cores, desc, dt = time_oracle(wl, seconds=args.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
+               "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+            "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "new_tokens": wl.n_tokens,
+                       "kv_history_tokens": int(wl.seen.sum()), "n_q_heads": wl.n_q_heads,
+                       "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim, "block_size": 64,
+                       "rope_theta": wl.rope_theta, "seed": wl.seed, "l2": l2_note,
+                       "parallelism": "replicas" if ws > 1 else "single"},
+            "roofline": roof,
+            "step_roofline_frac": step_frac,
+            "decode_kv_gbps": alg["kv_history_bytes"] / (float(np.mean(attn_ms)) / 1e3) / 1e9,
+            "append_ms": float(np.mean(app_ms)), "attention_ms": float(np.mean(attn_ms)),
+            "algorithmic": {"flops": alg["flops"], "bytes": alg["bytes"]},
+            "hbm_frac_vs_8tbs": (alg["attn_bytes"] / attn_mean_s / 1e9) / 8000.0,
+            "meta_build_us": meta_build_us,
+            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches_per_step * K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = W.make_workload(args.workload, args.seed)
+    if args.impl == "reference":
+        return reference_arm(args, wl)
+    return gpu_arm(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,250 @@
+/*
+ * ds_ragged.h -- C ABI of the ragged blocked-KV attention layer for one GB300
+ * (sm_103a): rotary embedding + KV-cache append, then causal attention of every
+ * new token over its sequence's whole history read through integer block ids.
+ *
+ * Source of the design ("DeepSpeed Inference v2", pyshine.com/deepspeed-2):
+ *  - section "Ragged batches: packing a whole server into four tensors": the
+ *    tokens of all in-flight sequences are concatenated into one stream with
+ *    per-sequence metadata in parallel buffers (RaggedBatchWrapper's
+ *    insert_sequence packs host buffers, finalize uploads them with a few
+ *    non-blocking copies); kernels read block ids from the metadata and address
+ *    the KV pools directly, so one kernel serves any batch composition;
+ *    attention runs over per-head work "atoms" (AtomBuilder) in a blocked flash
+ *    attention kernel (BlockedFlashAttn).
+ *  - section "The front desk": a DSSequenceDescriptor keeps the integer block
+ *    ids of its sequence; BlockedKVCache pools are flat block-indexed tensors;
+ *    the allocator's discipline makes overflow impossible to hide; scheduling
+ *    answers with a result instead of throwing.
+ *  - "DeepSpeed-Inference and DeepSpeed-MII" tutorial (jwzheng96, ch. 10),
+ *    section 10.3: Dynamic SplitFuse mixes prefill chunks and single-token
+ *    decodes in one batch; engine limits max_ragged_sequence_count = 256 and
+ *    max_ragged_batch_size = 8192 (used as default capacities by callers, not
+ *    hard-coded: every capacity is an argument).
+ *
+ * Conventions (all calls):
+ *  - The library never allocates device or pinned memory and owns no stream.
+ *    Every buffer is the caller's; sizes come from the *_size functions.
+ *  - Device calls are asynchronous on the caller's stream.  Argument errors
+ *    are found on the host before anything is enqueued and returned as a
+ *    ds_status; nothing is thrown and nothing traps.  ds_last_error() gives a
+ *    one-line message for the calling thread.
+ *  - Kernels also check every block id and position they use; a violation sets
+ *    a device error word (read by ds_get_device_error) and skips the access.
+ *  - Storage types: IEEE fp16 or bfloat16 (DS_FP16, DS_BF16).
+ */
+#ifndef DS_RAGGED_H
+#define DS_RAGGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status -- */
+typedef int32_t ds_status;
+#define DS_OK 0
+#define DS_ERR_INVALID_ARG 1  /* null pointer, misaligned buffer, bad field   */
+#define DS_ERR_CAPACITY 2     /* over a capacity, or a block list too short   */
+#define DS_ERR_BAD_BLOCK 3    /* block id outside the pool, or used twice     */
+#define DS_ERR_UNSUPPORTED 4  /* head_dim, block_size, dtype or head ratio    */
+#define DS_ERR_WORKSPACE 5    /* a caller buffer is smaller than required     */
+#define DS_ERR_CUDA 6         /* a CUDA runtime call failed                   */
+
+/* Device error word bits (ds_get_device_error). */
+#define DS_DEVERR_BLOCK_ID 1  /* a kernel met a block id outside the pool     */
+#define DS_DEVERR_POSITION 2  /* a position beyond the rotary table or blocks */
+#define DS_DEVERR_WORKLIST 4  /* an inconsistent work-list entry              */
+
+#define DS_FP16 0
+#define DS_BF16 1
+
+#define DS_ROPE_HALF 0        /* pairs (x_k, x_{k+d/2})  (default)            */
+#define DS_ROPE_INTERLEAVED 1 /* pairs (x_{2k}, x_{2k+1})                     */
+
+/* Thread-local message describing the last non-DS_OK status of this thread. */
+const char* ds_last_error(void);
+
+/* ------------------------------------------------------------ descriptors -- */
+
+/* One sequence of the batch (the DSSequenceDescriptor of the pages): tokens
+ * already in the cache, tokens in this forward pass, and the integer block ids
+ * it owns, in order (HOST memory, read during the call only).  A sequence uses
+ * its first ceil((seen+new)/block_size) ids; extra ids are ignored; fewer is
+ * DS_ERR_CAPACITY.  new_tokens >= 1, seen_tokens >= 0. */
+typedef struct ds_seq_desc {
+    int32_t seen_tokens;
+    int32_t new_tokens;
+    const int32_t* block_ids;
+    int32_t n_blocks;
+} ds_seq_desc;
+
+/* Layer shape.  Supported: head_dim 64 or 128, block_size 64, n_q_heads a
+ * multiple of n_kv_heads with g = n_q_heads/n_kv_heads in {1,2,4,8,16};
+ * rope_theta > 0; softmax_scale <= 0 selects 1/sqrt(head_dim).
+ * Query head h reads KV head floor(h / g). */
+typedef struct ds_attn_params {
+    int32_t n_q_heads;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    int32_t dtype;      /* DS_FP16 | DS_BF16 */
+    int32_t rope_style; /* DS_ROPE_HALF | DS_ROPE_INTERLEAVED */
+    float rope_theta;
+    float softmax_scale;
+} ds_attn_params;
+
+/* The block-indexed KV pool (one cache group of the BlockedKVCache).
+ * base: DEVICE, 16-byte aligned, layout [num_blocks][2][n_kv_heads][block_size]
+ * [head_dim] of the storage type: index 0 of the second axis holds rotated
+ * keys, index 1 values.  Each (block, K|V, head) tile is contiguous. */
+typedef struct ds_kv_pool {
+    void* base;
+    int32_t num_blocks;
+} ds_kv_pool;
+
+/* Rotary table: DEVICE float pairs (cos, sin) [max_positions][head_dim/2] for
+ * angle fp32(fp32(p) * fp32(theta^(-2k/d))), each rounded from fp64.  Built once
+ * per (theta, head_dim) by ds_rope_table_build, like any per-model constant. */
+typedef struct ds_rope_table {
+    const void* table;
+    int32_t max_positions;
+    int32_t head_dim;
+    float rope_theta;
+} ds_rope_table;
+
+/* Ragged batch metadata (the RaggedBatchWrapper's buffers).
+ * Caller fills the first group and keeps it; ds_ragged_meta_build fills the
+ * rest on every batch. */
+typedef struct ds_ragged_meta {
+    /* --- set by the caller (ds_meta_buffer_sizes gives the byte counts) --- */
+    void* device_buf;     /* DEVICE, 256-byte aligned                        */
+    size_t device_bytes;
+    void* host_staging;   /* HOST (pinned for an asynchronous upload)        */
+    size_t staging_bytes;
+    int32_t max_seqs;
+    int32_t max_tokens;
+    int32_t max_blocks;   /* capacity of the packed block table              */
+    /* --- filled by ds_ragged_meta_build --- */
+    int32_t n_seqs;
+    int32_t n_tokens;
+    int32_t n_blocks;     /* entries of the packed block table               */
+    int32_t n_prefill_seqs;
+    int32_t n_decode_seqs;
+    int32_t n_prefill_tiles;
+    int32_t n_decode_items;
+    int32_t max_len;      /* max over sequences of seen + new                */
+    int32_t pool_num_blocks;
+    int32_t split_blocks; /* KV blocks per decode split                      */
+    size_t used_bytes;    /* bytes uploaded                                  */
+    /* DEVICE pointers into device_buf (int32 unless noted):
+     *   header[16]        word 0: device error bits, 1: S, 2: N, 3: blocks
+     *   cu_seqlens[S+1]   exclusive prefix sum of new_tokens
+     *   seq_seen[S], seq_new[S]
+     *   blk_off[S+1]      exclusive prefix sum of ceil((seen+new)/block_size)
+     *   block_table[n_blocks]  each sequence's used ids, in batch order
+     *   tok_seq[N]        sequence index of each packed token
+     *   tok_pos[N]        position seen_i + j of each packed token
+     *   prefill_tiles     int4 {seq, first token j0, tokens in tile, kv_len}
+     *                     kv_len = keys the tile's last row attends to
+     *   decode_items      int4 {seq, first block, end block, partial slot}
+     *   decode_seqs       int4 {seq, token, first item, item count} */
+    int32_t* header;
+    int32_t* cu_seqlens;
+    int32_t* seq_seen;
+    int32_t* seq_new;
+    int32_t* blk_off;
+    int32_t* block_table;
+    int32_t* tok_seq;
+    int32_t* tok_pos;
+    int32_t* prefill_tiles;
+    int32_t* decode_items;
+    int32_t* decode_seqs;
+} ds_ragged_meta;
+
+/* ------------------------------------------------------------------ calls -- */
+
+/* Byte counts for a metadata device buffer and its host staging buffer that
+ * hold any batch within the capacities.  Returns DS_ERR_INVALID_ARG on
+ * negative capacities, DS_ERR_UNSUPPORTED on an unsupported params. */
+ds_status ds_meta_buffer_sizes(int32_t max_seqs, int32_t max_tokens, int32_t max_blocks,
+                               const ds_attn_params* params, size_t* device_bytes,
+                               size_t* staging_bytes);
+
+/* Host half of ds_ragged_meta_build (no CUDA call): validate the descriptors
+ * and pack the metadata and the work lists into meta->host_staging; fill the
+ * host fields of *meta and its device pointers.  Validation order: argument
+ * pointers and params, then per sequence new_tokens >= 1 and seen >= 0
+ * (DS_ERR_INVALID_ARG), block list length and the capacities
+ * (DS_ERR_CAPACITY), block ids inside [0, pool_num_blocks) and no id used
+ * twice in the batch (DS_ERR_BAD_BLOCK). */
+ds_status ds_ragged_meta_pack(const ds_seq_desc* seqs, int32_t n_seqs,
+                              const ds_attn_params* params, int32_t pool_num_blocks,
+                              ds_ragged_meta* meta);
+
+/* RaggedBatchWrapper.insert_sequence + finalize: ds_ragged_meta_pack, then one
+ * cudaMemcpyAsync of meta->used_bytes from host_staging to device_buf on
+ * `stream`.  host_staging must stay untouched until the stream has passed
+ * this point.  stream is a cudaStream_t (0 = legacy default stream). */
+ds_status ds_ragged_meta_build(const ds_seq_desc* seqs, int32_t n_seqs,
+                               const ds_attn_params* params, int32_t pool_num_blocks,
+                               ds_ragged_meta* meta, void* stream);
+
+/* Bytes of a rotary table for positions [0, max_positions). */
+ds_status ds_rope_table_size(const ds_attn_params* params, int32_t max_positions,
+                             size_t* bytes);
+
+/* Fill a caller-allocated DEVICE table (16-byte aligned) and describe it in
+ * *out.  One kernel on `stream`; cos/sin evaluated in fp64 on the device. */
+ds_status ds_rope_table_build(const ds_attn_params* params, int32_t max_positions,
+                              void* table, size_t table_bytes, ds_rope_table* out,
+                              void* stream);
+
+/* Rotary embedding + KV append (one kernel).  For every packed token t
+ * (sequence i, position p = seen_i + j): rotate its key heads and store them,
+ * with its value heads unchanged, in slot (block_table_i[p / block_size],
+ * p % block_size) of the pool.  When q_out is not NULL also write the rotated
+ * query heads, storage-rounded, to q_out[N][n_q_heads*head_dim].
+ * qkv: DEVICE, 16-byte aligned, [N][(n_q_heads + 2*n_kv_heads)*head_dim], each
+ * row = query heads, then key heads, then value heads.  Not modified.
+ * Rotation per pair (x0, x1) with (c, s) from the table, all in fp32 and never
+ * fused: y0 = x0*c - x1*s, y1 = x1*c + x0*s; then round-to-nearest-even. */
+ds_status ds_kv_rotary_append(const ds_ragged_meta* meta, const ds_attn_params* params,
+                              const ds_rope_table* rope, const void* qkv, void* q_out,
+                              const ds_kv_pool* pool, void* stream);
+
+/* Workspace bytes ds_blocked_attention needs for any batch within the
+ * capacities (decode split partials). */
+ds_status ds_blocked_attention_workspace_size(const ds_attn_params* params, int32_t max_seqs,
+                                              int32_t max_tokens, int32_t max_blocks,
+                                              size_t* bytes);
+
+/* Blocked causal attention (BlockedFlashAttn over the work atoms): for every
+ * packed token t of sequence i at position p and every query head h,
+ *   out[t][h] = sum_{u<=p} softmax_u(scale * <rot(q_t,h), K[u]>) V[u]
+ * with K, V read from the pool through the sequence's block table, KV head
+ * floor(h/g), and the query rotated on load (fp32, same rule as the append).
+ * Must follow ds_kv_rotary_append of the same batch on the same stream.
+ * Prefill tiles (sequences with new_tokens > 1) run on tensor cores; decode
+ * rows (new_tokens == 1) run a split-K kernel over KV blocks and a combine.
+ * out: DEVICE, 16-byte aligned, [N][n_q_heads*head_dim].  workspace: DEVICE,
+ * 256-byte aligned, ws_bytes >= ds_blocked_attention_workspace_size. */
+ds_status ds_blocked_attention(const ds_ragged_meta* meta, const ds_attn_params* params,
+                               const ds_rope_table* rope, const void* qkv,
+                               const ds_kv_pool* pool, void* out, void* workspace,
+                               size_t ws_bytes, void* stream);
+
+/* Wait for `stream` and read the device error word of the last batch built in
+ * *meta (0 = none; DS_DEVERR_* bits otherwise). */
+ds_status ds_get_device_error(const ds_ragged_meta* meta, int32_t* err, void* stream);
+
+/* Library version string. */
+const char* ds_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS_RAGGED_H */

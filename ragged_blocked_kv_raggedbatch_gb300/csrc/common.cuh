@@ -1,0 +1,205 @@
+// common.cuh -- internal helpers shared by the library's kernels and host code.
+//
+// Nothing here is part of the C ABI (include/ds_ragged.h is).  The metadata
+// layout constants below define how ds_ragged_meta_pack lays out the device
+// buffer that the kernels read.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ds_ragged.h"
+
+namespace dsr {
+
+// ---------------------------------------------------------------- metadata --
+// Header words of the device metadata buffer.
+enum : int {
+  HDR_ERR = 0,       // device error bits (DS_DEVERR_*), zero after every upload
+  HDR_S = 1,
+  HDR_N = 2,
+  HDR_BLOCKS = 3,
+  HDR_WORDS = 16,
+};
+
+constexpr int kBlockSize = 64;        // tokens per KV block (only supported value)
+constexpr int kPrefillRows = 64;      // rows (tokens x heads of one KV group) per prefill tile
+constexpr int kMinSplitBlocks = 4;    // smallest decode split, in KV blocks
+constexpr int kMaxSplitBlocks = 16;
+
+// Kernel arguments that every launch needs, resolved on the host.
+struct LayerArgs {
+  int32_t Hq, Hkv, D, G, dtype, style;
+  float scale_log2;        // softmax scale * log2(e)
+  int32_t num_blocks;      // pool size
+  int32_t max_positions;   // rotary table rows
+  const float2* rope;      // [max_positions][D/2]
+  int32_t* header;         // device error word lives at header[HDR_ERR]
+};
+
+// ----------------------------------------------------------- device helpers --
+#ifdef __CUDACC__
+
+__device__ __forceinline__ void set_dev_error(int32_t* header, int bits) {
+  atomicOr(reinterpret_cast<int*>(header + HDR_ERR), bits);
+}
+
+// Storage <-> fp32 (exact up-conversion; round-to-nearest-even down).
+template <bool BF16> struct Stor;
+template <> struct Stor<true> {
+  __device__ __forceinline__ static float lo(uint32_t w) { return __uint_as_float(w << 16); }
+  __device__ __forceinline__ static float hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+  __device__ __forceinline__ static uint32_t pack(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+  }
+};
+template <> struct Stor<false> {
+  __device__ __forceinline__ static float lo(uint32_t w) {
+    float f;
+    asm("{ .reg .f16 h; mov.b32 {h, _}, %1; cvt.f32.f16 %0, h; }" : "=f"(f) : "r"(w));
+    return f;
+  }
+  __device__ __forceinline__ static float hi(uint32_t w) {
+    float f;
+    asm("{ .reg .f16 h; mov.b32 {_, h}, %1; cvt.f32.f16 %0, h; }" : "=f"(f) : "r"(w));
+    return f;
+  }
+  __device__ __forceinline__ static uint32_t pack(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+  }
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Rotation of one pair in fp32 with every product and sum rounded separately
+// (never contracted into a fused multiply-add):
+//   y0 = x0*c - x1*s,  y1 = x1*c + x0*s.
+__device__ __forceinline__ void rope_pair(float x0, float x1, float c, float s, float& y0,
+                                          float& y1) {
+  y0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
+  y1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, s));
+}
+
+// Rotate 8 pairs.  HALF: a holds x[8c..8c+7], b holds x[d/2+8c..]; the pair of
+// element e is (a[e], b[e]) with table index 8c+e.  INTERLEAVED: a, b hold
+// x[16c..16c+15]; pairs are adjacent elements, table index 8c + e.
+template <bool BF16, bool HALF>
+__device__ __forceinline__ void rotate16(uint4& a, uint4& b, const float4* cs /* 4 x float4 */) {
+  uint32_t* A = reinterpret_cast<uint32_t*>(&a);
+  uint32_t* B = reinterpret_cast<uint32_t*>(&b);
+  float c[8], s[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float4 v = cs[q];
+    c[2 * q] = v.x;
+    s[2 * q] = v.y;
+    c[2 * q + 1] = v.z;
+    s[2 * q + 1] = v.w;
+  }
+  if (HALF) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      float x0l = Stor<BF16>::lo(A[w]), x0h = Stor<BF16>::hi(A[w]);
+      float x1l = Stor<BF16>::lo(B[w]), x1h = Stor<BF16>::hi(B[w]);
+      float y0l, y1l, y0h, y1h;
+      rope_pair(x0l, x1l, c[2 * w], s[2 * w], y0l, y1l);
+      rope_pair(x0h, x1h, c[2 * w + 1], s[2 * w + 1], y0h, y1h);
+      A[w] = Stor<BF16>::pack(y0l, y0h);
+      B[w] = Stor<BF16>::pack(y1l, y1h);
+    }
+  } else {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      float y0, y1;
+      rope_pair(Stor<BF16>::lo(A[w]), Stor<BF16>::hi(A[w]), c[w], s[w], y0, y1);
+      A[w] = Stor<BF16>::pack(y0, y1);
+      rope_pair(Stor<BF16>::lo(B[w]), Stor<BF16>::hi(B[w]), c[4 + w], s[4 + w], y0, y1);
+      B[w] = Stor<BF16>::pack(y0, y1);
+    }
+  }
+}
+
+// ------------------------------------------------ mbarrier + bulk async copy --
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after ~`limit_cycles` SM
+// cycles.  Returns false on timeout (the caller records an error and stops
+// issuing work; it never spins forever).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  long long limit_cycles = 4000000000LL) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit_cycles) return false;
+  }
+  return true;
+}
+
+// One bulk (non-tensor) global -> shared copy completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+#endif  // __CUDACC__
+
+// -------------------------------------------------------------- launchers --
+// Implemented in the .cu files; called by the host layer after validation.
+cudaError_t launch_rope_table(const ds_attn_params& p, int32_t max_positions, float2* table,
+                              cudaStream_t st);
+cudaError_t launch_append(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
+                          void* q_out, void* pool, cudaStream_t st);
+cudaError_t launch_decode(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
+                          const void* pool, void* out, float* ws, cudaStream_t st);
+cudaError_t launch_prefill(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
+                           const void* pool, void* out, cudaStream_t st);
+
+}  // namespace dsr

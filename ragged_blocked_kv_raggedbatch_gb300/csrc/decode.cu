@@ -1,0 +1,404 @@
+// decode.cu -- blocked attention for decode rows (sequences with one new
+// token): split-K over KV blocks plus a combine step.
+//
+// A decode row reads its sequence's whole KV history once, so the kernel is
+// bound by HBM bandwidth.  Each CTA owns one (split, KV head) work atom: a run
+// of up to split_blocks KV blocks of one sequence ("DeepSpeed Inference v2",
+// pyshine.com/deepspeed-2, section "Ragged batches": attention runs over
+// per-head work atoms built from the batch metadata; kernels read block ids and
+// address the pools directly).  The CTA streams the (block, K|V, head) tiles,
+// each contiguous in the pool, into shared memory with bulk asynchronous copies
+// (TMA engine) completing on mbarriers, and all G query heads of the KV group
+// are scored against each loaded tile, so K/V are read from HBM once.
+//
+// Thread mapping: a key is handled by D/8 lanes holding 8 dimensions each
+// (16-byte shared-memory loads, conflict-free).  Each warp keeps its own online
+// softmax state over a fixed slice of every block; the warps' states are
+// merged at the end of the split.  A split emits (m, l, o[D]) per query head
+// in fp32 (m in log2 units), or the final row when it is its sequence's only
+// split; the combine kernel merges the splits of the others.
+#include "common.cuh"
+
+namespace dsr {
+
+constexpr float kNegBig = -1.0e30f;  // finite "minus infinity" for running maxima
+
+template <bool BF16>
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = Stor<BF16>::lo(w[i]);
+    f[2 * i + 1] = Stor<BF16>::hi(w[i]);
+  }
+}
+
+template <bool BF16, bool HALF, int D, int G, int WARPS, int STAGES>
+struct DecodeCfg {
+  static constexpr int LPK = D / 8;             // lanes per key
+  static constexpr int KPS = 32 / LPK;          // key groups per warp
+  static constexpr int KPW = kBlockSize / WARPS; // keys per warp per block
+  static constexpr int KPG = KPW / KPS;         // keys per group per block
+  static constexpr int REP = LPK / KPG;         // lanes holding the same reduced key
+  static constexpr int TILE_BYTES = kBlockSize * D * 2;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int PBUF_FLOATS = KPS * KPG * G;  // per warp
+  static constexpr int MERGE_FLOATS = WARPS * G * (D + 2);
+  static constexpr int TILES_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = TILES_BYTES;
+  static constexpr int PBUF_OFF = BAR_OFF + 8 * STAGES;
+  static constexpr int SMEM_BYTES = PBUF_OFF + WARPS * PBUF_FLOATS * 4;
+  static_assert(KPG >= 1 && KPG <= LPK, "key split");
+  static_assert(MERGE_FLOATS * 4 <= TILES_BYTES, "merge scratch aliases the tiles");
+};
+
+template <bool BF16, bool HALF, int D, int G, int WARPS, int STAGES>
+__global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(
+    const int4* __restrict__ items, const int32_t* __restrict__ cu_seqlens,
+    const int32_t* __restrict__ seq_seen, const int32_t* __restrict__ blk_off,
+    const int32_t* __restrict__ block_table, const uint16_t* __restrict__ qkv,
+    const uint16_t* __restrict__ pool, uint16_t* __restrict__ out, float* __restrict__ ws,
+    int32_t n_items, LayerArgs a) {
+  using C = DecodeCfg<BF16, HALF, D, G, WARPS, STAGES>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int grp = lane / C::LPK;       // key group inside the warp
+  const int li = lane % C::LPK;        // lane inside the group: dims [8*li, 8*li+8)
+  const int4 it = items[blockIdx.x];
+  const int seq = it.x, b_begin = it.y, b_end = it.z, slot = it.w;
+  const int c = blockIdx.y;            // KV head
+  const int t = cu_seqlens[seq];       // the row's packed token
+  const int p = seq_seen[seq];         // its position
+  const int L = p + 1;
+  const int nblk = b_end - b_begin;
+  const int* btab = block_table + blk_off[seq];
+  if (nblk <= 0 || p >= a.max_positions) {
+    if (tid == 0) set_dev_error(a.header, nblk <= 0 ? DS_DEVERR_WORKLIST : DS_DEVERR_POSITION);
+    return;
+  }
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  auto issue = [&](int stage, int b) {
+    int blk = btab[b];
+    uint64_t* bar = &bars[stage];
+    if (blk < 0 || blk >= a.num_blocks) {
+      set_dev_error(a.header, DS_DEVERR_BLOCK_ID);
+      mbar_arrive_expect_tx(bar, 0);  // complete the phase without data
+      return;
+    }
+    const uint16_t* kt = pool + (((int64_t)blk * 2 + 0) * a.Hkv + c) * (int64_t)(kBlockSize * D);
+    const uint16_t* vt = pool + (((int64_t)blk * 2 + 1) * a.Hkv + c) * (int64_t)(kBlockSize * D);
+    uint8_t* dst = smem + stage * C::STAGE_BYTES;
+    mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+    bulk_g2s(dst, kt, C::TILE_BYTES, bar);
+    bulk_g2s(dst + C::TILE_BYTES, vt, C::TILE_BYTES, bar);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < STAGES && s < nblk; ++s) issue(s, b_begin + s);
+  }
+
+  // ---- query: rotate (fp32, same rule as the append), scale into log2 units.
+  float q[G][8];
+  {
+    const uint16_t* qrow = qkv + (int64_t)t * (a.Hq + 2 * a.Hkv) * D;
+    const float2* cs = a.rope + (int64_t)p * (D / 2);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      uint4 raw = ld_nc_v4(qrow + (c * G + h) * D + 8 * li);
+      float x[8];
+      unpack8<BF16>(raw, x);
+      if (HALF) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = __shfl_xor_sync(0xffffffffu, x[e], C::LPK / 2);
+        const bool first = li < C::LPK / 2;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float2 r = cs[8 * (li % (C::LPK / 2)) + e];
+          float y0, y1;
+          if (first) rope_pair(x[e], y[e], r.x, r.y, y0, y1);
+          else rope_pair(y[e], x[e], r.x, r.y, y1, y0);
+          q[h][e] = y0 * a.scale_log2;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float2 r = cs[4 * li + e];
+          float y0, y1;
+          rope_pair(x[2 * e], x[2 * e + 1], r.x, r.y, y0, y1);
+          q[h][2 * e] = y0 * a.scale_log2;
+          q[h][2 * e + 1] = y1 * a.scale_log2;
+        }
+      }
+    }
+  }
+
+  float m[G], l[G], o[G][8];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = kNegBig;
+    l[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+  }
+  float* pbuf = reinterpret_cast<float*>(smem + C::PBUF_OFF) + warp * C::PBUF_FLOATS;
+  const int key0 = warp * C::KPW + grp * C::KPG;  // first key of this group in a block
+  const int my_key = (li / C::REP) % C::KPG;        // key this lane holds after reduction
+  bool timed_out = false;
+
+  for (int j = 0; j < nblk; ++j) {
+    const int stage = j % STAGES;
+    bool ok = mbar_wait_bounded(&bars[stage], (j / STAGES) & 1);
+    if (__syncthreads_or(!ok)) {
+      timed_out = true;
+      break;
+    }
+    const uint16_t* Kt = reinterpret_cast<const uint16_t*>(smem + stage * C::STAGE_BYTES);
+    const uint16_t* Vt = Kt + kBlockSize * D;
+    const int kbase = (b_begin + j) * kBlockSize;
+
+    // scores of this group's KPG keys, partial over the lane's 8 dims
+    float part[G][C::KPG];
+#pragma unroll
+    for (int i = 0; i < C::KPG; ++i) {
+      uint4 raw = *reinterpret_cast<const uint4*>(Kt + (key0 + i) * D + 8 * li);
+      float k8[8];
+      unpack8<BF16>(raw, k8);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(q[h][e], k8[e], acc);
+        part[h][i] = acc;
+      }
+    }
+    // transposed reduction over the group's lanes: halve the key set at each
+    // level (upper half to lanes with the level's bit set), then finish the sum.
+    float s[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float v[C::KPG];
+#pragma unroll
+      for (int i = 0; i < C::KPG; ++i) v[i] = part[h][i];
+#pragma unroll
+      for (int n = C::KPG, mask = C::LPK / 2; n > 1; n >>= 1, mask >>= 1) {
+        const bool upper = (li & mask) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+          float send = upper ? v[i] : v[i + n / 2];
+          float keep = upper ? v[i + n / 2] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+        }
+      }
+#pragma unroll
+      for (int mask = C::REP / 2; mask >= 1; mask >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
+      s[h] = (kbase + key0 + my_key < L) ? v[0] : -INFINITY;
+    }
+    // online softmax over the warp's keys of this block
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float mx = s[h];
+#pragma unroll
+      for (int mask = C::REP; mask < 32; mask <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, mask));
+      const float m_new = fmaxf(m[h], mx);
+      const float alpha = fast_exp2(m[h] - m_new);
+      const float pv = fast_exp2(s[h] - m_new);
+      float sum = pv;
+#pragma unroll
+      for (int mask = C::REP; mask < 32; mask <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, mask);
+      l[h] = l[h] * alpha + sum;
+      m[h] = m_new;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[h][e] *= alpha;
+      if ((li % C::REP) == 0) pbuf[(grp * C::KPG + my_key) * G + h] = pv;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < C::KPG; ++i) {
+      // slots past the sequence's length may hold non-finite bytes: skip them
+      if (kbase + key0 + i >= L) break;
+      uint4 raw = *reinterpret_cast<const uint4*>(Vt + (key0 + i) * D + 8 * li);
+      float v8[8];
+      unpack8<BF16>(raw, v8);
+      const float* pr = pbuf + (grp * C::KPG + i) * G;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float pw = pr[h];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pw, v8[e], o[h][e]);
+      }
+    }
+    __syncthreads();  // every warp is done with this stage and with pbuf
+    if (tid == 0 && j + STAGES < nblk) issue(stage, b_begin + j + STAGES);
+  }
+
+  if (timed_out) {
+    if (tid == 0) {
+      set_dev_error(a.header, DS_DEVERR_WORKLIST);
+      // let copies still in flight land before the CTA's memory is released
+      for (int s = 0; s < STAGES; ++s) (void)mbar_wait_bounded(&bars[s], 0, 100000000LL);
+    }
+    return;
+  }
+
+  // ---- merge the key groups of each warp (same m, l; o partial per group)
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+#pragma unroll
+      for (int mask = C::LPK; mask < 32; mask <<= 1) o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], mask);
+
+  // ---- merge the warps through shared memory (aliases the tile stages)
+  __syncthreads();
+  float* mg = reinterpret_cast<float*>(smem);  // [WARPS][G][D+2]
+  if (grp == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float* dst = mg + (warp * G + h) * (D + 2);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dst[8 * li + e] = o[h][e];
+      if (li == 0) {
+        dst[D] = m[h];
+        dst[D + 1] = l[h];
+      }
+    }
+  }
+  __syncthreads();
+  const int units = G * (D / 8);
+  for (int u = tid; u < units; u += WARPS * 32) {
+    const int h = u / (D / 8), d8 = u % (D / 8);
+    float M = kNegBig;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, mg[(w * G + h) * (D + 2) + D]);
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+      const float* src = mg + (w * G + h) * (D + 2);
+      const float sc = fast_exp2(src[D] - M);
+      lsum += sc * src[D + 1];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += sc * src[8 * d8 + e];
+    }
+    const int hq = c * G + h;
+    if (slot < 0) {
+      const float inv = 1.f / lsum;
+      uint4 pk;
+      uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pw[e] = Stor<BF16>::pack(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+      *reinterpret_cast<uint4*>(out + (int64_t)t * a.Hq * D + hq * D + 8 * d8) = pk;
+    } else {
+      float* wml = ws + ((int64_t)slot * a.Hq + hq) * 2;
+      float* wo = ws + (int64_t)n_items * a.Hq * 2 + ((int64_t)slot * a.Hq + hq) * D + 8 * d8;
+      if (d8 == 0) {
+        wml[0] = M;
+        wml[1] = lsum;
+      }
+      *reinterpret_cast<float4*>(wo) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      *reinterpret_cast<float4*>(wo + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+  }
+}
+
+// Merge the splits of each multi-split decode row: one warp per (row, head).
+template <bool BF16, int D>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const int4* __restrict__ dseqs,
+                                                             const float* __restrict__ ws,
+                                                             uint16_t* __restrict__ out,
+                                                             int32_t n_items, int32_t Hq) {
+  constexpr int DPL = D / 32;  // dims per lane: 4 or 2
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
+  if (h >= Hq) return;
+  const int4 ds = dseqs[blockIdx.x];
+  const int t = ds.y, first = ds.z, cnt = ds.w;
+  if (cnt <= 1) return;
+  float M = kNegBig;
+  for (int k = 0; k < cnt; ++k) M = fmaxf(M, ws[((int64_t)(first + k) * Hq + h) * 2]);
+  float acc[DPL];
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+  float lsum = 0.f;
+  const float* wo = ws + (int64_t)n_items * Hq * 2;
+  for (int k = 0; k < cnt; ++k) {
+    const float* ml = ws + ((int64_t)(first + k) * Hq + h) * 2;
+    const float sc = fast_exp2(ml[0] - M);
+    lsum += sc * ml[1];
+    const float* src = wo + ((int64_t)(first + k) * Hq + h) * D + DPL * lane;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[e] += sc * src[e];
+  }
+  const float inv = 1.f / lsum;
+  uint16_t* dst = out + (int64_t)t * Hq * D + h * D + DPL * lane;
+  if (DPL == 4) {
+    uint2 pk;
+    pk.x = Stor<BF16>::pack(acc[0] * inv, acc[1] * inv);
+    pk.y = Stor<BF16>::pack(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = pk;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = Stor<BF16>::pack(acc[0] * inv, acc[1] * inv);
+  }
+}
+
+template <bool BF16, bool HALF, int D, int G>
+static cudaError_t launch_decode_t(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
+                                   const void* pool, void* out, float* ws, cudaStream_t st) {
+  constexpr int WARPS = 4, STAGES = 3;
+  using C = DecodeCfg<BF16, HALF, D, G, WARPS, STAGES>;
+  auto kern = decode_split_kernel<BF16, HALF, D, G, WARPS, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid(m.n_decode_items, a.Hkv);
+  kern<<<grid, WARPS * 32, C::SMEM_BYTES, st>>>(
+      reinterpret_cast<const int4*>(m.decode_items), m.cu_seqlens, m.seq_seen, m.blk_off,
+      m.block_table, static_cast<const uint16_t*>(qkv), static_cast<const uint16_t*>(pool),
+      static_cast<uint16_t*>(out), ws, m.n_decode_items, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (m.n_decode_items > m.n_decode_seqs) {
+    dim3 g2(m.n_decode_seqs, (a.Hq + 3) / 4);
+    decode_combine_kernel<BF16, D><<<g2, 128, 0, st>>>(
+        reinterpret_cast<const int4*>(m.decode_seqs), ws, static_cast<uint16_t*>(out),
+        m.n_decode_items, a.Hq);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+template <bool BF16, bool HALF, int D>
+static cudaError_t launch_decode_g(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
+                                   const void* pool, void* out, float* ws, cudaStream_t st) {
+  switch (a.G) {
+    case 1: return launch_decode_t<BF16, HALF, D, 1>(m, a, qkv, pool, out, ws, st);
+    case 2: return launch_decode_t<BF16, HALF, D, 2>(m, a, qkv, pool, out, ws, st);
+    case 4: return launch_decode_t<BF16, HALF, D, 4>(m, a, qkv, pool, out, ws, st);
+    case 8: return launch_decode_t<BF16, HALF, D, 8>(m, a, qkv, pool, out, ws, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <bool BF16, bool HALF>
+static cudaError_t launch_decode_d(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
+                                   const void* pool, void* out, float* ws, cudaStream_t st) {
+  return a.D == 128 ? launch_decode_g<BF16, HALF, 128>(m, a, qkv, pool, out, ws, st)
+                    : launch_decode_g<BF16, HALF, 64>(m, a, qkv, pool, out, ws, st);
+}
+
+cudaError_t launch_decode(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
+                          const void* pool, void* out, float* ws, cudaStream_t st) {
+  const bool half = a.style == DS_ROPE_HALF;
+  if (a.dtype == DS_BF16)
+    return half ? launch_decode_d<true, true>(m, a, qkv, pool, out, ws, st)
+                : launch_decode_d<true, false>(m, a, qkv, pool, out, ws, st);
+  return half ? launch_decode_d<false, true>(m, a, qkv, pool, out, ws, st)
+              : launch_decode_d<false, false>(m, a, qkv, pool, out, ws, st);
+}
+
+}  // namespace dsr
