@@ -40,17 +40,23 @@ METRIC = "ragged attn new tokens/s per layer"
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic per launch of the dominant launches from an ncu capture, keyed
-# by workload, valid only while the kernel source hashes match.
-NCU_TRAFFIC = {}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
+# the dominant kernel from an ncu capture, keyed by workload; reported only
+# while the hash of the kernel's source files still matches the capture.
+NCU_TRAFFIC = {
+    # decode_split_kernel on the first 64 sequences of the decode-only batch:
+    # 2.290086 GB read + 8.07 MB written for 2.2576 GB algorithmic; scaled to the
+    # full batch by its algorithmic bytes (traffic grows with the KV read).
+    "decode256_mha_d128": {"bytes": 9.386e9, "files": ["decode.cu", "common.cuh"],
+                           "src": "e6d66d237bd04dbd"},
+}
 
 
-def _src_hash() -> str:
+def _src_hash(files) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ragged_blocked_kv_raggedbatch_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".cpp")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in files:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -346,7 +352,7 @@ def gpu_arm(args, wl):
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"]}
     rec = NCU_TRAFFIC.get(wl.name)
-    roof["traffic"] = rec["bytes"] if rec and rec.get("src") == _src_hash() else None
+    roof["traffic"] = rec["bytes"] if rec and rec.get("src") == _src_hash(rec["files"]) else None
     roof["kernel"] = "ds_blocked_attention launches (%s)" % (
         "decode split-K + combine" if m.n_prefill_tiles == 0 else
         "prefill tiles" if m.n_decode_items == 0 else "prefill tiles + decode split-K + combine")
@@ -427,6 +433,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--subset", type=int, default=0,
+                    help="profile a smaller case: only the first N sequences, compact pool")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -435,6 +443,8 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     wl = W.make_workload(args.workload, args.seed)
+    if args.subset:
+        wl = W.first_sequences(wl, args.subset, args.seed)
     if args.impl == "reference":
         return reference_arm(args, wl)
     return gpu_arm(args, wl)

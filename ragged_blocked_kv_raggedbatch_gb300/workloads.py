@@ -239,3 +239,16 @@ def subset(wl: RaggedWorkload, seq_idx: Sequence[int], name: Optional[str] = Non
     return dataclasses.replace(wl, name=name or (wl.name + "_subset"), seen=wl.seen[idx].copy(),
                                new=wl.new[idx].copy(),
                                block_ids=[wl.block_ids[i].copy() for i in idx])
+
+
+def first_sequences(wl: RaggedWorkload, n: int, seed: int = 0) -> RaggedWorkload:
+    """The first n sequences of a workload over a pool of exactly their blocks
+    (a seeded permutation of fresh ids): a smaller case of the same shape."""
+    n = min(n, wl.n_seqs)
+    rng = np.random.Generator(np.random.PCG64(seed + 1))
+    seen, new = wl.seen[:n].copy(), wl.new[:n].copy()
+    need = int(((seen.astype(np.int64) + new + wl.block_size - 1) // wl.block_size).sum())
+    ids = rng.permutation(need).astype(np.int32)
+    return dataclasses.replace(wl, name="%s_first%d" % (wl.name, n), seen=seen, new=new,
+                               block_ids=_assign_blocks(seen, new, wl.block_size, ids),
+                               num_blocks=need)
