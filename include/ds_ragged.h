@@ -236,6 +236,41 @@ ds_status ds_blocked_attention(const ds_ragged_meta* meta, const ds_attn_params*
                                const ds_kv_pool* pool, void* out, void* workspace,
                                size_t ws_bytes, void* stream);
 
+/* Allocation-free variant of ds_blocked_attention.  (The source pages have no
+ * counterpart: this entry point exists for callers that cannot allocate.)
+ *
+ * ds_blocked_attention needs a caller-provided workspace for the partial
+ * results of split decode rows.  Some callers cannot obtain one: a plugin
+ * loaded into a host application that owns all device memory through its own
+ * allocator and hands the plugin no way to allocate; a latency-critical loop
+ * in which a cudaMalloc, which may synchronize the device, is not acceptable;
+ * a deployment that reserves a fixed device-memory budget at start-up and may
+ * not allocate afterwards.  This entry point takes the same inputs and
+ * outputs (the caller still passes qkv, the pool and out) but keeps the split
+ * partials in a scratch array compiled into the library instead of a
+ * workspace argument.  It calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ *
+ * Limits and behaviour:
+ *  - The scratch array is DS_STATIC_WORKSPACE_BYTES (32 MiB) of device memory,
+ *    held on every GPU that loads the library until the process exits.  A
+ *    batch whose split partials need more (n_decode_items * n_q_heads *
+ *    (head_dim + 2) * 4 bytes) is rejected with DS_ERR_WORKSPACE before
+ *    anything is enqueued.
+ *  - The first call on each device (with that device current) looks up the
+ *    array's device address once; make that first call before any stream
+ *    capture begins.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents.  Nothing in it has to start at zero (every partial is written
+ *    before it is read), so it is never cleared.  Calls whose work overlaps
+ *    on the GPU (different streams, or several host threads) race on the
+ *    array: the caller must order them, e.g. on one stream.
+ * Arguments, errors and results are otherwise those of ds_blocked_attention. */
+#define DS_STATIC_WORKSPACE_BYTES ((size_t)32 << 20)
+ds_status ds_blocked_attention_static_ws(const ds_ragged_meta* meta, const ds_attn_params* params,
+                                         const ds_rope_table* rope, const void* qkv,
+                                         const ds_kv_pool* pool, void* out, void* stream);
+
 /* Wait for `stream` and read the device error word of the last batch built in
  * *meta (0 = none; DS_DEVERR_* bits otherwise). */
 ds_status ds_get_device_error(const ds_ragged_meta* meta, int32_t* err, void* stream);

@@ -191,6 +191,9 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
 
 #endif  // __CUDACC__
 
+// Records the message ds_last_error() returns on this thread (host.cpp).
+void set_last_error(const char* msg);
+
 // -------------------------------------------------------------- launchers --
 // Implemented in the .cu files; called by the host layer after validation.
 cudaError_t launch_rope_table(const ds_attn_params& p, int32_t max_positions, float2* table,

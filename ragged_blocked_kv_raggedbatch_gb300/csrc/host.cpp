@@ -138,6 +138,11 @@ ds_status check_pool(const ds_kv_pool* pool, const ds_ragged_meta* m) {
 
 }  // namespace
 
+namespace dsr {
+// Lets other translation units of the library record a ds_last_error message.
+void set_last_error(const char* msg) { std::snprintf(g_err, sizeof g_err, "%s", msg); }
+}  // namespace dsr
+
 extern "C" {
 
 const char* ds_last_error(void) { return g_err; }

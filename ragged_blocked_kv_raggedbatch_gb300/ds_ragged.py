@@ -75,7 +75,10 @@ SIGNATURES = {
     "ds_blocked_attention_workspace_size": (i32, [P, i32, i32, i32, P]),
     "ds_blocked_attention": (i32, [P, P, P, P, P, P, P, ctypes.c_size_t, P]),
     "ds_get_device_error": (i32, [P, P, P]),
+    "ds_blocked_attention_static_ws": (i32, [P, P, P, P, P, P, P]),
 }
+
+DS_STATIC_WORKSPACE_BYTES = 32 << 20
 
 _lib = None
 
@@ -214,6 +217,15 @@ def ds_blocked_attention(meta: ds_ragged_meta, params: ds_attn_params, rope: ds_
     _check(load().ds_blocked_attention(_ref(meta), _ref(params), _ref(rope), _ptr(qkv), _ref(pool),
                                        _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)),
            "ds_blocked_attention")
+
+
+def ds_blocked_attention_static_ws(meta: ds_ragged_meta, params: ds_attn_params, rope: ds_rope_table,
+                                   qkv, pool: ds_kv_pool, out, stream=None):
+    """ds_blocked_attention with the split partials in the library's built-in
+    scratch array (no workspace argument; nothing is allocated)."""
+    _check(load().ds_blocked_attention_static_ws(_ref(meta), _ref(params), _ref(rope), _ptr(qkv),
+                                                 _ref(pool), _ptr(out), _stream(stream)),
+           "ds_blocked_attention_static_ws")
 
 
 def ds_get_device_error(meta: ds_ragged_meta, stream=None) -> int:
