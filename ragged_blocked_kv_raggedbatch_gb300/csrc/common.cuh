@@ -23,7 +23,7 @@ enum : int {
 };
 
 constexpr int kBlockSize = 64;        // tokens per KV block (only supported value)
-constexpr int kPrefillRows = 64;      // rows (tokens x heads of one KV group) per prefill tile
+constexpr int kPrefillRows = 256;     // rows (tokens x heads of one KV group) per prefill atom
 constexpr int kMinSplitBlocks = 4;    // smallest decode split, in KV blocks
 constexpr int kMaxSplitBlocks = 16;
 

@@ -1,0 +1,451 @@
+// prefill_tc.cu -- blocked causal attention for prefill chunks on the 5th-gen
+// tensor cores (tcgen05 MMAs with accumulators in tensor memory, K/V tiles
+// staged by tiled TMA loads).
+//
+// Work atom ("DeepSpeed Inference v2", pyshine.com/deepspeed-2, section "Ragged
+// batches": AtomBuilder atoms executed by BlockedFlashAttn, q-block size chosen
+// per head size): one CTA owns up to 256/G consecutive new tokens of one
+// sequence and one KV head c, as two Q tiles of 128 rows (tokens x the G query
+// heads that read KV head c).  Both tiles share every 128-key K/V tile, which
+// is two 64-token pool blocks fetched through the block table.
+//
+// Roles (10 warps):
+//   warp 0      TMA producer: K/V tiles into a 2-stage ring (one KV tile ahead);
+//               zeroes the rows of the final V tile past the chunk's last key
+//               (those slots may hold anything and 0 * NaN would poison P*V).
+//   warp 1      tensor-memory owner and MMA issuer (one thread):
+//                 S_X = Q_X K_t^T   (SS MMA, 128 x 128 x D)
+//                 O_X += P_X V_t    (TS MMA: P read from tensor memory)
+//               issued as QK_A(0) QK_B(0) | PV_A(t) QK_A(t+1) PV_B(t) QK_B(t+1) ...
+//               so one tile's softmax overlaps the other tile's MMAs.
+//   warps 2-5   softmax of tile A, warps 6-9 softmax of tile B: one thread per
+//               row (tensor-memory lane = row); builds its Q row (rotated on
+//               load, fp32, same rule as the append) in 128-byte-swizzled shared
+//               memory; per KV tile: masked row max, conditional rescale of O
+//               (only when the max grows by more than 2^8: the reference max may
+//               lag, the final O / l is exact), P = exp2(S - m) written back over
+//               S as packed 16-bit pairs; epilogue O / l -> out.
+// Tensor memory: S_A [0,128) S_B [128,256) O_A [256,256+D) O_B [256+D,256+2D).
+// Every mbarrier wait is bounded: on timeout the CTA records an error and stops.
+#include <mutex>
+
+#include "tc.cuh"
+
+namespace dsr {
+
+template <int D>
+struct PfCfg {
+  static constexpr int ROWS = 128;
+  static constexpr int KEYS = 128;
+  static constexpr int HALVES = D / 64;
+  static constexpr int QHALF = ROWS * 128;      // one 64-column chunk of a Q tile
+  static constexpr int KHALF = KEYS * 128;      // one 64-column chunk of a K or V tile
+  static constexpr int QTILE = HALVES * QHALF;
+  static constexpr int KVTILE = HALVES * KHALF;
+  static constexpr int BOX_BYTES = 64 * 128;    // one TMA box: 64 keys x 64 elements
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = 2 * QTILE;
+  static constexpr int OFF_BAR = OFF_KV + 2 * 2 * KVTILE;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static constexpr int COL_S0 = 0, COL_O0 = 256;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int THREADS = 320;
+};
+
+enum {
+  B_QREADY = 0, B_KFULL = 1, B_VFULL = 3, B_KVEMPTY = 5, B_SFULL = 7, B_PFULL = 9,
+  B_ODONE = 11, B_VLAST = 13, B_DONE = 14, B_COUNT = 15
+};
+
+template <bool BF16, bool HALF, int D, int G>
+__global__ void __launch_bounds__(320, 1) prefill_tc_kernel(
+    const __grid_constant__ CUtensorMap pool_map, const int4* __restrict__ tiles,
+    const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ seq_seen,
+    const int32_t* __restrict__ blk_off, const int32_t* __restrict__ block_table,
+    const uint16_t* __restrict__ qkv, uint16_t* __restrict__ out, LayerArgs a) {
+  using C = PfCfg<D>;
+  constexpr int T = 128 / G;  // tokens per Q tile
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u = smem_u32(smem_raw);
+  uint8_t* sm = smem_raw + (((raw_u + 1023u) & ~1023u) - raw_u);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * B_COUNT);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int4 tl = tiles[blockIdx.x];
+  const int seq = tl.x, j0 = tl.y, ntok = tl.z, kv_len = tl.w;
+  const int c = blockIdx.y;
+  const int s_seen = seq_seen[seq];
+  const int tok0 = cu_seqlens[seq] + j0;
+  const int* btab = block_table + blk_off[seq];
+  if (ntok <= 0 || ntok > 2 * T || kv_len != s_seen + j0 + ntok) {
+    if (tid == 0) set_dev_error(a.header, DS_DEVERR_WORKLIST);
+    return;
+  }
+  if (kv_len > a.max_positions) {
+    if (tid == 0) set_dev_error(a.header, DS_DEVERR_POSITION);
+    return;
+  }
+  const bool has_b = ntok > T;
+  const int n_kv = (kv_len + C::KEYS - 1) / C::KEYS;
+
+  if (tid == 0) {
+    mbar_init(&bar[B_QREADY], 256);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar[B_KFULL + s], 1);
+      mbar_init(&bar[B_VFULL + s], 1);
+      mbar_init(&bar[B_KVEMPTY + s], 1);
+      mbar_init(&bar[B_SFULL + s], 1);
+      mbar_init(&bar[B_PFULL + s], 128);
+      mbar_init(&bar[B_ODONE + s], 1);
+    }
+    mbar_init(&bar[B_VLAST], 1);
+    mbar_init(&bar[B_DONE], 256);
+    fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  uint8_t* sQ = sm + C::OFF_Q;
+  uint8_t* sKV = sm + C::OFF_KV;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint32_t box_tx = C::HALVES * C::BOX_BYTES;
+    for (int t = 0; t < n_kv; ++t) {
+      const int st = t & 1;
+      if (t >= 2 && !mbar_wait_bounded(&bar[B_KVEMPTY + st], ((t >> 1) - 1) & 1)) {
+        if (lane == 0) set_dev_error(a.header, DS_DEVERR_WORKLIST);
+        break;
+      }
+      const bool has1 = t * C::KEYS + 64 < kv_len;
+      uint8_t* kdst = sKV + st * 2 * C::KVTILE;
+      uint8_t* vdst = kdst + C::KVTILE;
+      const bool last_partial = (t == n_kv - 1) && (kv_len % C::KEYS != 0);
+      uint64_t* vbar = last_partial ? &bar[B_VLAST] : &bar[B_VFULL + st];
+      if (lane == 0) {
+        const uint32_t tx = (has1 ? 2u : 1u) * box_tx;
+        mbar_arrive_expect_tx(&bar[B_KFULL + st], tx);
+        mbar_arrive_expect_tx(vbar, tx);
+        for (int i = 0; i < (has1 ? 2 : 1); ++i) {
+          int blk = btab[2 * t + i];
+          if (blk < 0 || blk >= a.num_blocks) {
+            set_dev_error(a.header, DS_DEVERR_BLOCK_ID);
+            blk = 0;
+          }
+          const int krow = ((blk * 2 + 0) * a.Hkv + c) * 64;
+          const int vrow = ((blk * 2 + 1) * a.Hkv + c) * 64;
+#pragma unroll
+          for (int h = 0; h < C::HALVES; ++h) {
+            tc::tma_load_2d(kdst + h * C::KHALF + i * C::BOX_BYTES, &pool_map, h * 64, krow,
+                            &bar[B_KFULL + st]);
+            tc::tma_load_2d(vdst + h * C::KHALF + i * C::BOX_BYTES, &pool_map, h * 64, vrow,
+                            vbar);
+          }
+        }
+      }
+      if (last_partial) {
+        if (!mbar_wait_bounded(&bar[B_VLAST], 0)) {
+          if (lane == 0) set_dev_error(a.header, DS_DEVERR_WORKLIST);
+          break;
+        }
+        const int first_bad = kv_len - t * C::KEYS;  // rows [first_bad, 128) hold no key
+        const int n16 = (C::KEYS - first_bad) * 8;   // 16-byte chunks per half
+        for (int h = 0; h < C::HALVES; ++h)
+          for (int i = lane; i < n16; i += 32)
+            *reinterpret_cast<uint4*>(vdst + h * C::KHALF + first_bad * 128 + i * 16) =
+                make_uint4(0, 0, 0, 0);
+        tc::fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[B_VFULL + st]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IQK = tc::idesc_f16(BF16, 128, 128, false);
+      constexpr uint32_t IPV = tc::idesc_f16(BF16, 128, D, true);
+      bool ok = mbar_wait_bounded(&bar[B_QREADY], 0);
+      auto qk = [&](int x, int t) {
+        const uint32_t qa = smem_u32(sQ + x * C::QTILE);
+        const uint32_t kb = smem_u32(sKV + (t & 1) * 2 * C::KVTILE);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t oq = (ks / 4) * C::QHALF + (ks % 4) * 32;
+          const uint32_t ok_ = (ks / 4) * C::KHALF + (ks % 4) * 32;
+          tc::mma_ss(tmem + C::COL_S0 + 128 * x, tc::smem_desc_sw128(qa + oq, 16, 1024),
+                     tc::smem_desc_sw128(kb + ok_, 16, 1024), IQK, ks > 0);
+        }
+        tc::mma_commit(&bar[B_SFULL + x]);
+      };
+      auto pv = [&](int x, int t) {
+        const uint32_t vb = smem_u32(sKV + (t & 1) * 2 * C::KVTILE + C::KVTILE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc::mma_ts(tmem + C::COL_O0 + D * x, tmem + C::COL_S0 + 128 * x + 8 * kk,
+                     tc::smem_desc_sw128(vb + kk * 2048, C::KHALF, 1024), IPV, (t > 0 || kk > 0));
+        tc::mma_commit(&bar[B_ODONE + x]);
+      };
+      if (ok) ok = mbar_wait_bounded(&bar[B_KFULL], 0);
+      if (ok) {
+        tc::fence_after();
+        qk(0, 0);
+        if (has_b) qk(1, 0);
+      }
+      for (int t = 0; ok && t < n_kv; ++t) {
+        const int st = t & 1;
+        ok = mbar_wait_bounded(&bar[B_VFULL + st], (t >> 1) & 1) &&
+             mbar_wait_bounded(&bar[B_PFULL + 0], t & 1);
+        if (!ok) break;
+        tc::fence_after();
+        pv(0, t);
+        if (t + 1 < n_kv) {
+          ok = mbar_wait_bounded(&bar[B_KFULL + (st ^ 1)], ((t + 1) >> 1) & 1);
+          if (!ok) break;
+          tc::fence_after();
+          qk(0, t + 1);
+        }
+        if (has_b) {
+          ok = mbar_wait_bounded(&bar[B_PFULL + 1], t & 1);
+          if (!ok) break;
+          tc::fence_after();
+          pv(1, t);
+        }
+        tc::mma_commit(&bar[B_KVEMPTY + st]);
+        if (has_b && t + 1 < n_kv) qk(1, t + 1);
+      }
+      if (!ok) set_dev_error(a.header, DS_DEVERR_WORKLIST);
+    }
+    __syncwarp();
+    // free tensor memory once every softmax thread has read its last values
+    (void)mbar_wait_bounded(&bar[B_DONE], 0);
+    __syncwarp();
+    tc::fence_after();
+    tc::tmem_dealloc(tmem, C::TMEM_COLS);
+    tc::tmem_relinquish();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int x = (warp - 2) >> 2;            // 0: tile A, 1: tile B
+    const int r = 32 * (warp & 3) + lane;     // row = tensor-memory lane
+    const int jt = x * T + r / G;             // token of this row inside the atom
+    const bool valid = jt < ntok;
+    const int head = c * G + r % G;
+    const int pos = s_seen + j0 + min(jt, ntok - 1);
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t col_s = C::COL_S0 + 128 * x;
+    const uint32_t col_o = C::COL_O0 + D * x;
+
+    // Q row: rotate on load, round to the storage type, 128-byte swizzle.
+    {
+      uint8_t* qt = sQ + x * C::QTILE;
+      const float4* cs4 = reinterpret_cast<const float4*>(a.rope) + (int64_t)pos * (D / 4);
+      const uint16_t* src = qkv + (int64_t)(tok0 + min(jt, ntok - 1)) * ((a.Hq + 2 * a.Hkv) * D) + head * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 16; ++cc) {
+        const int ch0 = HALF ? cc : 2 * cc;
+        const int ch1 = HALF ? D / 16 + cc : 2 * cc + 1;
+        uint4 x0 = make_uint4(0, 0, 0, 0), x1 = make_uint4(0, 0, 0, 0);
+        if (valid && (x == 0 || has_b)) {
+          x0 = ld_nc_v4(src + 8 * ch0);
+          x1 = ld_nc_v4(src + 8 * ch1);
+          float4 cs[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) cs[q] = __ldg(cs4 + 4 * cc + q);
+          rotate16<BF16, HALF>(x0, x1, cs);
+        }
+        *reinterpret_cast<uint4*>(qt + (ch0 / 8) * C::QHALF + r * 128 + (((ch0 % 8) ^ (r & 7)) << 4)) = x0;
+        *reinterpret_cast<uint4*>(qt + (ch1 / 8) * C::QHALF + r * 128 + (((ch1 % 8) ^ (r & 7)) << 4)) = x1;
+      }
+      tc::fence_proxy_async();
+      tc::mbar_arrive(&bar[B_QREADY]);
+    }
+
+    if (x == 0 || has_b) {
+      float m_ref = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int t = 0; t < n_kv; ++t) {
+        if (!mbar_wait_bounded(&bar[B_SFULL + x], t & 1)) { ok = false; break; }
+        tc::fence_after();
+        const int kbase = t * C::KEYS;
+        const bool need_mask = kbase + C::KEYS - 1 > pos;
+        uint32_t v[32];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          tc::tmem_ld32(lane_addr + col_s + 32 * ch, v);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float sv = __uint_as_float(v[e]) * a.scale_log2;
+            if (need_mask && kbase + 32 * ch + e > pos) sv = -INFINITY;
+            mx = fmaxf(mx, sv);
+          }
+        }
+        if (t == 0) {
+          m_ref = mx;
+        } else {
+          if (!mbar_wait_bounded(&bar[B_ODONE + x], (t - 1) & 1)) { ok = false; break; }
+          tc::fence_after();
+          // tensor-memory loads/stores are warp-collective: rescale as a warp
+          // whenever any of its rows needs it (alpha = 1 for the others)
+          const bool mine = mx > m_ref + 8.0f;
+          if (__any_sync(0xffffffffu, mine)) {
+            const float alpha = mine ? fast_exp2(m_ref - mx) : 1.0f;
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+              tc::tmem_ld32(lane_addr + col_o + 32 * ch, v);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+              tc::tmem_st32(lane_addr + col_o + 32 * ch, v);
+            }
+            tc::tmem_wait_st();
+            if (mine) {
+              l *= alpha;
+              m_ref = mx;
+            }
+          }
+        }
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          tc::tmem_ld32(lane_addr + col_s + 32 * ch, v);
+          tc::tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float s0 = __uint_as_float(v[2 * e]) * a.scale_log2;
+            float s1 = __uint_as_float(v[2 * e + 1]) * a.scale_log2;
+            if (need_mask) {
+              if (kbase + 32 * ch + 2 * e > pos) s0 = -INFINITY;
+              if (kbase + 32 * ch + 2 * e + 1 > pos) s1 = -INFINITY;
+            }
+            const float p0 = fast_exp2(s0 - m_ref), p1 = fast_exp2(s1 - m_ref);
+            l += p0 + p1;
+            pk[e] = Stor<BF16>::pack(p0, p1);
+          }
+          tc::tmem_st16(lane_addr + col_s + 16 * ch, pk);
+        }
+        tc::tmem_wait_st();
+        tc::fence_before();
+        tc::mbar_arrive(&bar[B_PFULL + x]);
+      }
+      if (ok && mbar_wait_bounded(&bar[B_ODONE + x], (n_kv - 1) & 1)) {
+        tc::fence_after();
+        const float inv = 1.f / l;
+        uint16_t* dst = out + (int64_t)(tok0 + jt) * a.Hq * D + head * D;
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t v[32];
+          tc::tmem_ld32(lane_addr + col_o + 32 * ch, v);
+          tc::tmem_wait_ld();
+          if (valid) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = Stor<BF16>::pack(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(dst + 32 * ch + 8 * q) =
+                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+      } else {
+        set_dev_error(a.header, DS_DEVERR_WORKLIST);
+      }
+    }
+    tc::fence_before();
+    tc::mbar_arrive(&bar[B_DONE]);
+  }
+}
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// The pool as a 2-D tensor [num_blocks*2*Hkv*64 rows][D]: row
+// ((blk*2 + kv)*Hkv + head)*64 + offset; boxes of 64 rows x 64 elements with
+// 128-byte swizzle.
+cudaError_t make_pool_map(CUtensorMap* map, const void* pool, const LayerArgs& a) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)a.D, (cuuint64_t)a.num_blocks * 2 * a.Hkv * 64};
+  cuuint64_t strides[1] = {(cuuint64_t)a.D * 2};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, a.dtype == DS_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  2, const_cast<void*>(pool), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+template <bool BF16, bool HALF, int D, int G>
+static cudaError_t launch_prefill_t(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
+                                    const void* pool, void* out, cudaStream_t st) {
+  using C = PfCfg<D>;
+  CUtensorMap map;
+  cudaError_t e = make_pool_map(&map, pool, a);
+  if (e != cudaSuccess) return e;
+  auto kern = prefill_tc_kernel<BF16, HALF, D, G>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid(m.n_prefill_tiles, a.Hkv);
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(map, reinterpret_cast<const int4*>(m.prefill_tiles),
+                                          m.cu_seqlens, m.seq_seen, m.blk_off, m.block_table,
+                                          static_cast<const uint16_t*>(qkv),
+                                          static_cast<uint16_t*>(out), a);
+  return cudaGetLastError();
+}
+
+template <bool BF16, bool HALF, int D>
+static cudaError_t launch_prefill_g(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
+                                    const void* pool, void* out, cudaStream_t st) {
+  switch (a.G) {
+    case 1: return launch_prefill_t<BF16, HALF, D, 1>(m, a, qkv, pool, out, st);
+    case 2: return launch_prefill_t<BF16, HALF, D, 2>(m, a, qkv, pool, out, st);
+    case 4: return launch_prefill_t<BF16, HALF, D, 4>(m, a, qkv, pool, out, st);
+    case 8: return launch_prefill_t<BF16, HALF, D, 8>(m, a, qkv, pool, out, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <bool BF16, bool HALF>
+static cudaError_t launch_prefill_d(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
+                                    const void* pool, void* out, cudaStream_t st) {
+  return a.D == 128 ? launch_prefill_g<BF16, HALF, 128>(m, a, qkv, pool, out, st)
+                    : launch_prefill_g<BF16, HALF, 64>(m, a, qkv, pool, out, st);
+}
+
+cudaError_t launch_prefill(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
+                           const void* pool, void* out, cudaStream_t st) {
+  const bool half = a.style == DS_ROPE_HALF;
+  if (a.dtype == DS_BF16)
+    return half ? launch_prefill_d<true, true>(m, a, qkv, pool, out, st)
+                : launch_prefill_d<true, false>(m, a, qkv, pool, out, st);
+  return half ? launch_prefill_d<false, true>(m, a, qkv, pool, out, st)
+              : launch_prefill_d<false, false>(m, a, qkv, pool, out, st);
+}
+
+}  // namespace dsr

@@ -86,7 +86,7 @@ def _check_coverage(wl, meta, got):
     """Every prefill token is covered by exactly one tile; every KV block of
     every decode row by exactly one split item; slots are unique."""
     g = wl.n_q_heads // wl.n_kv_heads
-    tile_tokens = 64 // g
+    tile_tokens = 256 // g
     cover = {}
     kv_prev = None
     for seq, j0, nt, kv in got["prefill_tiles"]:
