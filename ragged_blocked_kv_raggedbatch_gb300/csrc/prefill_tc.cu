@@ -9,7 +9,9 @@
 // heads that read KV head c).  Both tiles share every 128-key K/V tile, which
 // is two 64-token pool blocks fetched through the block table.
 //
-// Roles (10 warps):
+// Roles (12 warps = 3 warpgroups; launched at 168 registers a thread, the
+// first warpgroup gives registers back (setmaxnreg 80) and the two softmax
+// warpgroups take them (setmaxnreg 208): 128*80 + 2*128*208 <= 384*168):
 //   warp 0      TMA producer: K/V tiles into a 2-stage ring (one KV tile ahead);
 //               zeroes the rows of the final V tile past the chunk's last key
 //               (those slots may hold anything and 0 * NaN would poison P*V).
@@ -18,7 +20,8 @@
 //                 O_X += P_X V_t    (TS MMA: P read from tensor memory)
 //               issued as QK_A(0) QK_B(0) | PV_A(t) QK_A(t+1) PV_B(t) QK_B(t+1) ...
 //               so one tile's softmax overlaps the other tile's MMAs.
-//   warps 2-5   softmax of tile A, warps 6-9 softmax of tile B: one thread per
+//   warps 2-3   no work (they only return their registers)
+//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: one thread per
 //               row (tensor-memory lane = row); builds its Q row (rotated on
 //               load, fp32, same rule as the append) in 128-byte-swizzled shared
 //               memory; per KV tile: masked row max, conditional rescale of O
@@ -49,7 +52,7 @@ struct PfCfg {
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static constexpr int COL_S0 = 0, COL_O0 = 256;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 384;
 };
 
 enum {
@@ -58,7 +61,7 @@ enum {
 };
 
 template <bool BF16, bool HALF, int D, int G>
-__global__ void __launch_bounds__(320, 1) prefill_tc_kernel(
+__global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
     const __grid_constant__ CUtensorMap pool_map, const int4* __restrict__ tiles,
     const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ seq_seen,
     const int32_t* __restrict__ blk_off, const int32_t* __restrict__ block_table,
@@ -112,7 +115,9 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(
   uint8_t* sQ = sm + C::OFF_Q;
   uint8_t* sKV = sm + C::OFF_KV;
 
-  if (warp == 0) {
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;\n" ::: "memory");
+    if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint32_t box_tx = C::HALVES * C::BOX_BYTES;
     for (int t = 0; t < n_kv; ++t) {
@@ -226,9 +231,11 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(
     tc::fence_after();
     tc::tmem_dealloc(tmem, C::TMEM_COLS);
     tc::tmem_relinquish();
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;\n" ::: "memory");
     // ------------------------------------------------------------ softmax
-    const int x = (warp - 2) >> 2;            // 0: tile A, 1: tile B
+    const int x = (warp - 4) >> 2;            // 0: tile A, 1: tile B
     const int r = 32 * (warp & 3) + lane;     // row = tensor-memory lane
     const int jt = x * T + r / G;             // token of this row inside the atom
     const bool valid = jt < ntok;
@@ -264,69 +271,77 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(
     }
 
     if (x == 0 || has_b) {
-      float m_ref = -INFINITY, l = 0.f;
+      float m_ref = -INFINITY, l = 0.f;  // m_ref in log2 units (scaled)
+      const float sc = a.scale_log2;
       bool ok = true;
       for (int t = 0; t < n_kv; ++t) {
         if (!mbar_wait_bounded(&bar[B_SFULL + x], t & 1)) { ok = false; break; }
         tc::fence_after();
+        // the whole S row of this KV tile, one wait
+        uint32_t v[128];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(lane_addr + col_s + 32 * ch, v + 32 * ch);
+        tc::tmem_wait_ld();
         const int kbase = t * C::KEYS;
-        const bool need_mask = kbase + C::KEYS - 1 > pos;
-        uint32_t v[32];
-        float mx = -INFINITY;
+        if (kbase + C::KEYS - 1 > pos) {  // diagonal tile: keys past this row's position
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          tc::tmem_ld32(lane_addr + col_s + 32 * ch, v);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float sv = __uint_as_float(v[e]) * a.scale_log2;
-            if (need_mask && kbase + 32 * ch + e > pos) sv = -INFINITY;
-            mx = fmaxf(mx, sv);
-          }
+          for (int e = 0; e < 128; ++e)
+            if (kbase + e > pos) v[e] = __float_as_uint(-INFINITY);
         }
+        // row max of the raw scores (scale > 0 commutes with max)
+        float m0 = __uint_as_float(v[0]), m1 = __uint_as_float(v[1]);
+        float m2 = __uint_as_float(v[2]), m3 = __uint_as_float(v[3]);
+#pragma unroll
+        for (int e = 4; e < 128; e += 8) {
+          m0 = tc::fmax3(m0, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+          m1 = tc::fmax3(m1, __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+          m2 = tc::fmax3(m2, __uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
+          m3 = tc::fmax3(m3, __uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+        }
+        const float mx = tc::fmax3(m0, m1, fmaxf(m2, m3)) * sc;
+        // keep the reference max unless the row max outgrows it by 2^8
+        bool mine = false;
+        float alpha = 1.0f;
         if (t == 0) {
           m_ref = mx;
-        } else {
+        } else if (mx > m_ref + 8.0f) {
+          mine = true;
+          alpha = fast_exp2(m_ref - mx);
+          m_ref = mx;
+        }
+        if (t > 0) {  // P(t) overwrites P(t-1); O must hold PV(t-1) before a rescale
           if (!mbar_wait_bounded(&bar[B_ODONE + x], (t - 1) & 1)) { ok = false; break; }
           tc::fence_after();
-          // tensor-memory loads/stores are warp-collective: rescale as a warp
-          // whenever any of its rows needs it (alpha = 1 for the others)
-          const bool mine = mx > m_ref + 8.0f;
-          if (__any_sync(0xffffffffu, mine)) {
-            const float alpha = mine ? fast_exp2(m_ref - mx) : 1.0f;
-#pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-              tc::tmem_ld32(lane_addr + col_o + 32 * ch, v);
-              tc::tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-              tc::tmem_st32(lane_addr + col_o + 32 * ch, v);
-            }
-            tc::tmem_wait_st();
-            if (mine) {
-              l *= alpha;
-              m_ref = mx;
-            }
-          }
         }
+        const float nm = -m_ref;
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          tc::tmem_ld32(lane_addr + col_s + 32 * ch, v);
-          tc::tmem_wait_ld();
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            float s0 = __uint_as_float(v[2 * e]) * a.scale_log2;
-            float s1 = __uint_as_float(v[2 * e + 1]) * a.scale_log2;
-            if (need_mask) {
-              if (kbase + 32 * ch + 2 * e > pos) s0 = -INFINITY;
-              if (kbase + 32 * ch + 2 * e + 1 > pos) s1 = -INFINITY;
-            }
-            const float p0 = fast_exp2(s0 - m_ref), p1 = fast_exp2(s1 - m_ref);
-            l += p0 + p1;
+            float y0, y1;
+            tc::ffma2(y0, y1, __uint_as_float(v[32 * ch + 2 * e]), __uint_as_float(v[32 * ch + 2 * e + 1]),
+                      sc, sc, nm, nm);
+            const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+            tc::fadd2(s0, s1, p0, p1);
             pk[e] = Stor<BF16>::pack(p0, p1);
           }
           tc::tmem_st16(lane_addr + col_s + 16 * ch, pk);
+        }
+        l = l * alpha + (s0 + s1);
+        // tensor-memory loads/stores are warp-collective: rescale O as a warp
+        // whenever any of its rows needs it (alpha = 1 for the others)
+        if (t > 0 && __any_sync(0xffffffffu, mine)) {
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t o[32];
+            tc::tmem_ld32(lane_addr + col_o + 32 * ch, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tc::tmem_st32(lane_addr + col_o + 32 * ch, o);
+          }
         }
         tc::tmem_wait_st();
         tc::fence_before();
