@@ -435,6 +435,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--subset", type=int, default=0,
                     help="profile a smaller case: only the first N sequences, compact pool")
+    ap.add_argument("--part", choices=["decode", "prefill"], default=None,
+                    help="profile one kernel family: keep only the decode rows or the prefill chunks")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -443,6 +445,9 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     wl = W.make_workload(args.workload, args.seed)
+    if args.part:
+        keep = [i for i in range(wl.n_seqs) if (wl.new[i] == 1) == (args.part == "decode")]
+        wl = W.compact_sequences(wl, keep, args.seed, suffix="_" + args.part)
     if args.subset:
         wl = W.first_sequences(wl, args.subset, args.seed)
     if args.impl == "reference":

@@ -2,6 +2,8 @@
 
 Each translation unit compiles in parallel; the result lands in
 ``ragged_blocked_kv_raggedbatch_gb300/_build/``.  Rebuilds only what changed.
+Extra nvcc flags (e.g. -D overrides of the decode CTA shape) can be given in
+the DSR_NVCC_FLAGS environment variable.
 """
 from __future__ import annotations
 
@@ -43,9 +45,12 @@ def _headers():
 def _compile(src: str, verbose_ptxas: bool) -> str:
     obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")
     newest_dep = max([os.path.getmtime(src)] + [os.path.getmtime(h) for h in _headers()])
-    if os.path.exists(obj) and os.path.getmtime(obj) >= newest_dep:
+    stamp = obj + ".flags"
+    extra = os.environ.get("DSR_NVCC_FLAGS", "")
+    same_flags = os.path.exists(stamp) and open(stamp).read() == extra
+    if os.path.exists(obj) and os.path.getmtime(obj) >= newest_dep and same_flags:
         return obj
-    flags = list(NVCC_FLAGS)
+    flags = list(NVCC_FLAGS) + os.environ.get("DSR_NVCC_FLAGS", "").split()
     if verbose_ptxas and src.endswith(".cu"):
         flags += ["-Xptxas", "-v"]
     cmd = [_nvcc()] + flags + ["-c", src, "-o", obj + ".tmp"]
@@ -55,6 +60,8 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     if verbose_ptxas:
         sys.stderr.write(r.stderr)
     os.replace(obj + ".tmp", obj)
+    with open(stamp, "w") as f:
+        f.write(extra)
     return obj
 
 

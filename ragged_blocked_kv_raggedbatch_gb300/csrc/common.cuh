@@ -200,8 +200,11 @@ cudaError_t launch_rope_table(const ds_attn_params& p, int32_t max_positions, fl
                               cudaStream_t st);
 cudaError_t launch_append(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
                           void* q_out, void* pool, cudaStream_t st);
+// overlap_previous: launch as a programmatic dependent of the kernel before it
+// on the stream (the prefill kernel), so decode CTAs can start while it runs.
 cudaError_t launch_decode(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                          const void* pool, void* out, float* ws, cudaStream_t st);
+                          const void* pool, void* out, float* ws, cudaStream_t st,
+                          bool overlap_previous);
 cudaError_t launch_prefill(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
                            const void* pool, void* out, cudaStream_t st);
 

@@ -17,7 +17,31 @@
 // merged at the end of the split.  A split emits (m, l, o[D]) per query head
 // in fp32 (m in log2 units), or the final row when it is its sequence's only
 // split; the combine kernel merges the splits of the others.
-#include "common.cuh"
+#include "tc.cuh"
+
+// CTA shape: warps per CTA, bulk-copy pipeline stages (each stage one K + V
+// tile pair, 32 KB at D=128) and CTAs per SM the registers must allow, for
+// G < 4 and G >= 4 query heads per KV head.  Measured on GB300 (decode rows of
+// the 2048-token SplitFuse batch, G=4): 4 warps x 2 stages x 3 CTAs/SM
+// 6.52 TB/s; 4 x 3 x 2: 5.63; 8 x 2 x 2: 5.35; 8 x 3 x 1: 3.69.
+#ifndef DSR_DECODE_WARPS
+#define DSR_DECODE_WARPS 4
+#endif
+#ifndef DSR_DECODE_STAGES
+#define DSR_DECODE_STAGES 2
+#endif
+#ifndef DSR_DECODE_WARPS_GQA
+#define DSR_DECODE_WARPS_GQA 4
+#endif
+#ifndef DSR_DECODE_STAGES_GQA
+#define DSR_DECODE_STAGES_GQA 2
+#endif
+#ifndef DSR_DECODE_MINB
+#define DSR_DECODE_MINB 3
+#endif
+#ifndef DSR_DECODE_MINB_GQA
+#define DSR_DECODE_MINB_GQA 3
+#endif
 
 namespace dsr {
 
@@ -53,7 +77,7 @@ struct DecodeCfg {
 };
 
 template <bool BF16, bool HALF, int D, int G, int WARPS, int STAGES>
-__global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(
+__global__ void __launch_bounds__(WARPS * 32, G >= 4 ? DSR_DECODE_MINB_GQA : DSR_DECODE_MINB) decode_split_kernel(
     const int4* __restrict__ items, const int32_t* __restrict__ cu_seqlens,
     const int32_t* __restrict__ seq_seen, const int32_t* __restrict__ blk_off,
     const int32_t* __restrict__ block_table, const uint16_t* __restrict__ qkv,
@@ -172,10 +196,10 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(
       unpack8<BF16>(raw, k8);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        float acc = 0.f;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc = fmaf(q[h][e], k8[e], acc);
-        part[h][i] = acc;
+        for (int e = 0; e < 8; e += 2) tc::ffma2(a0, a1, q[h][e], q[h][e + 1], k8[e], k8[e + 1], a0, a1);
+        part[h][i] = a0 + a1;
       }
     }
     // transposed reduction over the group's lanes: halve the key set at each
@@ -215,7 +239,7 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(
       l[h] = l[h] * alpha + sum;
       m[h] = m_new;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[h][e] *= alpha;
+      for (int e = 0; e < 8; e += 2) tc::fmul2(o[h][e], o[h][e + 1], alpha, alpha);
       if ((li % C::REP) == 0) pbuf[(grp * C::KPG + my_key) * G + h] = pv;
     }
     __syncwarp();
@@ -231,7 +255,8 @@ __global__ void __launch_bounds__(WARPS * 32) decode_split_kernel(
       for (int h = 0; h < G; ++h) {
         const float pw = pr[h];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pw, v8[e], o[h][e]);
+        for (int e = 0; e < 8; e += 2)
+          tc::ffma2(o[h][e], o[h][e + 1], v8[e], v8[e + 1], pw, pw, o[h][e], o[h][e + 1]);
       }
     }
     __syncthreads();  // every warp is done with this stage and with pbuf
@@ -349,17 +374,33 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const int4* __restr
 
 template <bool BF16, bool HALF, int D, int G>
 static cudaError_t launch_decode_t(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                                   const void* pool, void* out, float* ws, cudaStream_t st) {
-  constexpr int WARPS = 4, STAGES = 3;
+                                   const void* pool, void* out, float* ws, cudaStream_t st,
+                                   bool overlap_previous) {
+  constexpr int WARPS = G >= 4 ? DSR_DECODE_WARPS_GQA : DSR_DECODE_WARPS;
+  constexpr int STAGES = G >= 4 ? DSR_DECODE_STAGES_GQA : DSR_DECODE_STAGES;
   using C = DecodeCfg<BF16, HALF, D, G, WARPS, STAGES>;
   auto kern = decode_split_kernel<BF16, HALF, D, G, WARPS, STAGES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid(m.n_decode_items, a.Hkv);
-  kern<<<grid, WARPS * 32, C::SMEM_BYTES, st>>>(
-      reinterpret_cast<const int4*>(m.decode_items), m.cu_seqlens, m.seq_seen, m.blk_off,
-      m.block_table, static_cast<const uint16_t*>(qkv), static_cast<const uint16_t*>(pool),
-      static_cast<uint16_t*>(out), ws, m.n_decode_items, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(m.n_decode_items, a.Hkv);
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  // After the prefill kernel (which lets dependents start as soon as all its
+  // CTAs are running), decode CTAs may fill the SMs that prefill leaves idle:
+  // the two read only what the KV append wrote before either started and
+  // write disjoint output rows.
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_previous ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const int4*>(m.decode_items), m.cu_seqlens,
+                         m.seq_seen, m.blk_off, m.block_table, static_cast<const uint16_t*>(qkv),
+                         static_cast<const uint16_t*>(pool), static_cast<uint16_t*>(out), ws,
+                         (int32_t)m.n_decode_items, a);
+  if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (m.n_decode_items > m.n_decode_seqs) {
@@ -374,31 +415,33 @@ static cudaError_t launch_decode_t(const ds_ragged_meta& m, const LayerArgs& a, 
 
 template <bool BF16, bool HALF, int D>
 static cudaError_t launch_decode_g(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                                   const void* pool, void* out, float* ws, cudaStream_t st) {
+                                   const void* pool, void* out, float* ws, cudaStream_t st, bool ov) {
   switch (a.G) {
-    case 1: return launch_decode_t<BF16, HALF, D, 1>(m, a, qkv, pool, out, ws, st);
-    case 2: return launch_decode_t<BF16, HALF, D, 2>(m, a, qkv, pool, out, ws, st);
-    case 4: return launch_decode_t<BF16, HALF, D, 4>(m, a, qkv, pool, out, ws, st);
-    case 8: return launch_decode_t<BF16, HALF, D, 8>(m, a, qkv, pool, out, ws, st);
+    case 1: return launch_decode_t<BF16, HALF, D, 1>(m, a, qkv, pool, out, ws, st, ov);
+    case 2: return launch_decode_t<BF16, HALF, D, 2>(m, a, qkv, pool, out, ws, st, ov);
+    case 4: return launch_decode_t<BF16, HALF, D, 4>(m, a, qkv, pool, out, ws, st, ov);
+    case 8: return launch_decode_t<BF16, HALF, D, 8>(m, a, qkv, pool, out, ws, st, ov);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <bool BF16, bool HALF>
 static cudaError_t launch_decode_d(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                                   const void* pool, void* out, float* ws, cudaStream_t st) {
-  return a.D == 128 ? launch_decode_g<BF16, HALF, 128>(m, a, qkv, pool, out, ws, st)
-                    : launch_decode_g<BF16, HALF, 64>(m, a, qkv, pool, out, ws, st);
+                                   const void* pool, void* out, float* ws, cudaStream_t st, bool ov) {
+  return a.D == 128 ? launch_decode_g<BF16, HALF, 128>(m, a, qkv, pool, out, ws, st, ov)
+                    : launch_decode_g<BF16, HALF, 64>(m, a, qkv, pool, out, ws, st, ov);
 }
 
 cudaError_t launch_decode(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                          const void* pool, void* out, float* ws, cudaStream_t st) {
+                          const void* pool, void* out, float* ws, cudaStream_t st,
+                          bool overlap_previous) {
   const bool half = a.style == DS_ROPE_HALF;
+  const bool ov = overlap_previous;
   if (a.dtype == DS_BF16)
-    return half ? launch_decode_d<true, true>(m, a, qkv, pool, out, ws, st)
-                : launch_decode_d<true, false>(m, a, qkv, pool, out, ws, st);
-  return half ? launch_decode_d<false, true>(m, a, qkv, pool, out, ws, st)
-              : launch_decode_d<false, false>(m, a, qkv, pool, out, ws, st);
+    return half ? launch_decode_d<true, true>(m, a, qkv, pool, out, ws, st, ov)
+                : launch_decode_d<true, false>(m, a, qkv, pool, out, ws, st, ov);
+  return half ? launch_decode_d<false, true>(m, a, qkv, pool, out, ws, st, ov)
+              : launch_decode_d<false, false>(m, a, qkv, pool, out, ws, st, ov);
 }
 
 }  // namespace dsr

@@ -435,7 +435,8 @@ ds_status ds_blocked_attention(const ds_ragged_meta* meta, const ds_attn_params*
     if (e != cudaSuccess) return cuda_fail(e, "prefill kernel");
   }
   if (meta->n_decode_items > 0) {
-    cudaError_t e = dsr::launch_decode(*meta, a, qkv, pool->base, out, static_cast<float*>(workspace), st);
+    cudaError_t e = dsr::launch_decode(*meta, a, qkv, pool->base, out, static_cast<float*>(workspace), st,
+                                       meta->n_prefill_tiles > 0);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernels");
   }
   return DS_OK;

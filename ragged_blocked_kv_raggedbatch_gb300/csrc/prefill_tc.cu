@@ -91,6 +91,9 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
   }
   const bool has_b = ntok > T;
   const int n_kv = (kv_len + C::KEYS - 1) / C::KEYS;
+  // The decode launch that follows needs nothing from this kernel: let it
+  // start as soon as every CTA of this grid is running.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (tid == 0) {
     mbar_init(&bar[B_QREADY], 256);

@@ -150,6 +150,12 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
       : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1) {
+  asm("{ .reg .b64 a, d;\n mov.b64 a, {%2, %3};\n mov.b64 d, {%0, %1};\n mul.f32x2 d, d, a;\n"
+      " mov.b64 {%0, %1}, d; }"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
 __device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) {
   asm("{ .reg .b64 a, d;\n mov.b64 a, {%2, %3};\n mov.b64 d, {%0, %1};\n add.f32x2 d, d, a;\n"
       " mov.b64 {%0, %1}, d; }"

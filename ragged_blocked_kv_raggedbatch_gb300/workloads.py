@@ -241,14 +241,20 @@ def subset(wl: RaggedWorkload, seq_idx: Sequence[int], name: Optional[str] = Non
                                block_ids=[wl.block_ids[i].copy() for i in idx])
 
 
-def first_sequences(wl: RaggedWorkload, n: int, seed: int = 0) -> RaggedWorkload:
-    """The first n sequences of a workload over a pool of exactly their blocks
-    (a seeded permutation of fresh ids): a smaller case of the same shape."""
-    n = min(n, wl.n_seqs)
+def compact_sequences(wl: RaggedWorkload, keep: Sequence[int], seed: int = 0,
+                      suffix: str = "_part") -> RaggedWorkload:
+    """Some sequences of a workload over a pool of exactly their blocks (a
+    seeded permutation of fresh ids): a smaller case of the same shape."""
+    idx = np.asarray(list(keep), dtype=np.int64)
     rng = np.random.Generator(np.random.PCG64(seed + 1))
-    seen, new = wl.seen[:n].copy(), wl.new[:n].copy()
+    seen, new = wl.seen[idx].copy(), wl.new[idx].copy()
     need = int(((seen.astype(np.int64) + new + wl.block_size - 1) // wl.block_size).sum())
     ids = rng.permutation(need).astype(np.int32)
-    return dataclasses.replace(wl, name="%s_first%d" % (wl.name, n), seen=seen, new=new,
+    return dataclasses.replace(wl, name=wl.name + suffix, seen=seen, new=new,
                                block_ids=_assign_blocks(seen, new, wl.block_size, ids),
                                num_blocks=need)
+
+
+def first_sequences(wl: RaggedWorkload, n: int, seed: int = 0) -> RaggedWorkload:
+    """The first n sequences of a workload over a compact pool."""
+    return compact_sequences(wl, range(min(n, wl.n_seqs)), seed, suffix="_first%d" % min(n, wl.n_seqs))

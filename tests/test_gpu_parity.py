@@ -190,3 +190,28 @@ def test_device_error_word_on_inconsistent_metadata():
     layer.attention(qkv, pool, run.out)
     torch.cuda.synchronize()
     assert layer.device_error() & R.DS_DEVERR_BLOCK_ID
+
+
+def test_stream_order_after_overlapped_launches():
+    """The decode kernel may start while the prefill kernel still runs; work
+    enqueued after the attention call on the same stream must still see both
+    kernels' rows.  A long prefill chunk (slow) plus quick decodes, then an
+    ordinary copy of the output on the same stream right after the call."""
+    wl = W.make_custom([(20000, 256), (100, 1), (3000, 1), (64, 1)], 32, 8, 128, dtype="bf16",
+                       seed=12, extra_blocks=2)
+    qkv, pool = W.make_values(wl, "cuda")
+    nb = int(wl.blocks_needed().sum())
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        layer = R.RaggedLayer(R.params_for(wl), wl.n_seqs, wl.n_tokens, nb, wl.max_len(), stream=stream)
+        layer.build(R.SeqDescs.of(wl), wl.num_blocks)
+        layer.append(qkv, pool)
+        out = torch.full((wl.n_tokens, wl.n_q_heads * wl.head_dim), float("nan"), dtype=qkv.dtype,
+                         device="cuda")
+        for _ in range(3):
+            out.fill_(float("nan"))
+            layer.attention(qkv, pool, out)
+            snap = out.clone()  # an ordinary kernel right behind the call
+            stream.synchronize()
+            assert torch.isfinite(snap.float()).all()
+            assert torch.equal(snap.view(torch.int16), out.view(torch.int16))
