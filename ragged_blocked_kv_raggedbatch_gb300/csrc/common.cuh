@@ -25,7 +25,7 @@ enum : int {
 constexpr int kBlockSize = 64;        // tokens per KV block (only supported value)
 constexpr int kPrefillRows = 256;     // rows (tokens x heads of one KV group) per prefill atom
 constexpr int kMinSplitBlocks = 4;    // smallest decode split, in KV blocks
-constexpr int kMaxSplitBlocks = 16;
+constexpr int kMaxSplitBlocks = 32;   // largest decode split, in KV blocks
 
 // Kernel arguments that every launch needs, resolved on the host.
 struct LayerArgs {
