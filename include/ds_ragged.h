@@ -138,6 +138,8 @@ typedef struct ds_ragged_meta {
     int32_t max_len;      /* max over sequences of seen + new                */
     int32_t pool_num_blocks;
     int32_t split_blocks; /* KV blocks per decode split                      */
+    float prefill_sms;    /* SMs the prefill grid takes when decode rows run
+                             beside it (0: all SMs)                          */
     size_t used_bytes;    /* bytes uploaded                                  */
     /* DEVICE pointers into device_buf (int32 unless noted):
      *   header[16]        word 0: device error bits, 1: S, 2: N, 3: blocks

@@ -16,6 +16,10 @@
 
 #include "common.cuh"
 
+#ifndef DSR_PREFILL_SM_FACTOR
+#define DSR_PREFILL_SM_FACTOR 2.2
+#endif
+
 namespace {
 
 thread_local char g_err[512] = "";
@@ -334,6 +338,21 @@ ds_status ds_ragged_meta_pack(const ds_seq_desc* seqs, int32_t n_seqs,
   m->max_len = (int32_t)max_len;
   m->pool_num_blocks = pool_num_blocks;
   m->split_blocks = split;
+  // SMs for the persistent prefill grid when decode rows run beside it: enough
+  // for the prefill atoms to finish well within the time the decode rows take
+  // to stream their KV history.  Costs measured on GB300: ~1.8 us per 128-key
+  // step of a two-tile atom (1.2 us with one tile); decode KV at ~6.4 TB/s.
+  // The margin (DSR_PREFILL_SM_FACTOR) was swept on GB300: SplitFuse 2048 at
+  // 1.0 / 1.25 / 1.6 / 2.2: 2.08 / 1.79 / 1.59 / 1.35 ms.
+  m->prefill_sms = 0.f;
+  if (!tv.empty() && dec_blocks > 0) {
+    double pre_us = 0.0;
+    for (const Tile& t : tv)
+      pre_us += (double)((t.kv_len + 127) / 128) * (t.ntok > tile_tokens / 2 ? 1.8 : 1.2);
+    pre_us *= params->n_kv_heads;
+    const double dec_us = (double)dec_blocks * params->n_kv_heads * 2.0 * bs * params->head_dim * 2.0 / 6.4e6;
+    m->prefill_sms = (float)(DSR_PREFILL_SM_FACTOR * pre_us / dec_us);
+  }
   m->used_bytes = L.total * 4;
   int32_t* base = static_cast<int32_t*>(m->device_buf);
   m->header = base + L.hdr;

@@ -4,10 +4,12 @@
 //
 // Work atom ("DeepSpeed Inference v2", pyshine.com/deepspeed-2, section "Ragged
 // batches": AtomBuilder atoms executed by BlockedFlashAttn, q-block size chosen
-// per head size): one CTA owns up to 256/G consecutive new tokens of one
-// sequence and one KV head c, as two Q tiles of 128 rows (tokens x the G query
-// heads that read KV head c).  Both tiles share every 128-key K/V tile, which
-// is two 64-token pool blocks fetched through the block table.
+// per head size): up to 256/G consecutive new tokens of one sequence and one
+// KV head c, as two Q tiles of 128 rows (tokens x the G query heads that read
+// KV head c).  Both tiles share every 128-key K/V tile, which is two 64-token
+// pool blocks fetched through the block table.  The grid is persistent: CTA i
+// takes one atom per round of the longest-first list (snake order); the K/V ring,
+// barrier phases and tensor memory carry over from one atom to the next.
 //
 // Roles (12 warps = 3 warpgroups; launched at 168 registers a thread, the
 // first warpgroup gives registers back (setmaxnreg 80) and the two softmax
@@ -30,6 +32,8 @@
 //               S as packed 16-bit pairs; epilogue O / l -> out.
 // Tensor memory: S_A [0,128) S_B [128,256) O_A [256,256+D) O_B [256+D,256+2D).
 // Every mbarrier wait is bounded: on timeout the CTA records an error and stops.
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "tc.cuh"
@@ -56,13 +60,13 @@ struct PfCfg {
 };
 
 enum {
-  B_QREADY = 0, B_KFULL = 1, B_VFULL = 3, B_KVEMPTY = 5, B_SFULL = 7, B_PFULL = 9,
-  B_ODONE = 11, B_VLAST = 13, B_DONE = 14, B_COUNT = 15
+  B_QREADY = 0, B_KFULL = 2, B_VFULL = 4, B_KVEMPTY = 6, B_SFULL = 8, B_PFULL = 10,
+  B_ODONE = 12, B_VLAST = 14, B_DONE = 15, B_COUNT = 16
 };
 
 template <bool BF16, bool HALF, int D, int G>
 __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
-    const __grid_constant__ CUtensorMap pool_map, const int4* __restrict__ tiles,
+    const __grid_constant__ CUtensorMap pool_map, const int4* __restrict__ tiles, int32_t n_atoms,
     const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ seq_seen,
     const int32_t* __restrict__ blk_off, const int32_t* __restrict__ block_table,
     const uint16_t* __restrict__ qkv, uint16_t* __restrict__ out, LayerArgs a) {
@@ -73,31 +77,16 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
   uint8_t* sm = smem_raw + (((raw_u + 1023u) & ~1023u) - raw_u);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * B_COUNT);
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int4 tl = tiles[blockIdx.x];
-  const int seq = tl.x, j0 = tl.y, ntok = tl.z, kv_len = tl.w;
-  const int c = blockIdx.y;
-  const int s_seen = seq_seen[seq];
-  const int tok0 = cu_seqlens[seq] + j0;
-  const int* btab = block_table + blk_off[seq];
-  if (ntok <= 0 || ntok > 2 * T || kv_len != s_seen + j0 + ntok) {
-    if (tid == 0) set_dev_error(a.header, DS_DEVERR_WORKLIST);
-    return;
-  }
-  if (kv_len > a.max_positions) {
-    if (tid == 0) set_dev_error(a.header, DS_DEVERR_POSITION);
-    return;
-  }
-  const bool has_b = ntok > T;
-  const int n_kv = (kv_len + C::KEYS - 1) / C::KEYS;
-  // The decode launch that follows needs nothing from this kernel: let it
-  // start as soon as every CTA of this grid is running.
+
+  // Every CTA of this grid stays resident until the prefill work is done, so
+  // the decode launch that follows (it needs nothing from this kernel) may
+  // start at once on the SMs this grid does not use.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (tid == 0) {
-    mbar_init(&bar[B_QREADY], 256);
     for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar[B_QREADY + s], 128);
       mbar_init(&bar[B_KFULL + s], 1);
       mbar_init(&bar[B_VFULL + s], 1);
       mbar_init(&bar[B_KVEMPTY + s], 1);
@@ -114,171 +103,230 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-
   uint8_t* sQ = sm + C::OFF_Q;
   uint8_t* sKV = sm + C::OFF_KV;
+
+  // Atom k of the work list: prefill tile k / Hkv (longest first), KV head k % Hkv.
+  // CTA i takes one atom per round in snake order (round r: r*P + i for even
+  // r, r*P + P-1-i for odd r), which evens out the longest-first costs.  Each
+  // role walks the same atoms and skips the same malformed ones.
+  auto snake_atom = [&](int rnd) -> int {
+    const int P = gridDim.x, i = blockIdx.x;
+    return rnd * P + ((rnd & 1) ? (P - 1 - i) : i);
+  };
+  struct Atom {
+    int seq, j0, ntok, kv_len, c, s_seen, tok0, n_kv;
+    bool has_b;
+    const int* btab;
+  };
+  auto load_atom = [&](int k, Atom& at) -> bool {
+    const int4 tl = tiles[k / a.Hkv];
+    at.seq = tl.x; at.j0 = tl.y; at.ntok = tl.z; at.kv_len = tl.w;
+    at.c = k % a.Hkv;
+    at.s_seen = seq_seen[at.seq];
+    at.tok0 = cu_seqlens[at.seq] + at.j0;
+    at.btab = block_table + blk_off[at.seq];
+    at.has_b = at.ntok > T;
+    at.n_kv = (at.kv_len + C::KEYS - 1) / C::KEYS;
+    if (at.ntok <= 0 || at.ntok > 2 * T || at.kv_len != at.s_seen + at.j0 + at.ntok) {
+      if (tid == 0) set_dev_error(a.header, DS_DEVERR_WORKLIST);
+      return false;
+    }
+    if (at.kv_len > a.max_positions) {
+      if (tid == 0) set_dev_error(a.header, DS_DEVERR_POSITION);
+      return false;
+    }
+    return true;
+  };
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 80;\n" ::: "memory");
     if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    const uint32_t box_tx = C::HALVES * C::BOX_BYTES;
-    for (int t = 0; t < n_kv; ++t) {
-      const int st = t & 1;
-      if (t >= 2 && !mbar_wait_bounded(&bar[B_KVEMPTY + st], ((t >> 1) - 1) & 1)) {
-        if (lane == 0) set_dev_error(a.header, DS_DEVERR_WORKLIST);
-        break;
+      // ---------------------------------------------------------- producer
+      const uint32_t box_tx = C::HALVES * C::BOX_BYTES;
+      uint32_t ring = 0, vlast_uses = 0;
+      bool ok = true;
+      for (int rnd = 0, k = snake_atom(0); ok && k < n_atoms; k = snake_atom(++rnd)) {
+        Atom at;
+        if (!load_atom(k, at)) continue;
+        for (int t = 0; t < at.n_kv; ++t, ++ring) {
+          const int st = ring & 1;
+          if (ring >= 2 && !mbar_wait_bounded(&bar[B_KVEMPTY + st], ((ring >> 1) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          const bool has1 = t * C::KEYS + 64 < at.kv_len;
+          uint8_t* kdst = sKV + st * 2 * C::KVTILE;
+          uint8_t* vdst = kdst + C::KVTILE;
+          const bool last_partial = (t == at.n_kv - 1) && (at.kv_len % C::KEYS != 0);
+          uint64_t* vbar = last_partial ? &bar[B_VLAST] : &bar[B_VFULL + st];
+          if (lane == 0) {
+            const uint32_t tx = (has1 ? 2u : 1u) * box_tx;
+            mbar_arrive_expect_tx(&bar[B_KFULL + st], tx);
+            mbar_arrive_expect_tx(vbar, tx);
+            for (int i = 0; i < (has1 ? 2 : 1); ++i) {
+              int blk = at.btab[2 * t + i];
+              if (blk < 0 || blk >= a.num_blocks) {
+                set_dev_error(a.header, DS_DEVERR_BLOCK_ID);
+                blk = 0;
+              }
+              const int krow = ((blk * 2 + 0) * a.Hkv + at.c) * 64;
+              const int vrow = ((blk * 2 + 1) * a.Hkv + at.c) * 64;
+#pragma unroll
+              for (int h = 0; h < C::HALVES; ++h) {
+                tc::tma_load_2d(kdst + h * C::KHALF + i * C::BOX_BYTES, &pool_map, h * 64, krow,
+                                &bar[B_KFULL + st]);
+                tc::tma_load_2d(vdst + h * C::KHALF + i * C::BOX_BYTES, &pool_map, h * 64, vrow, vbar);
+              }
+            }
+          }
+          if (last_partial) {
+            if (!mbar_wait_bounded(&bar[B_VLAST], vlast_uses & 1)) {
+              ok = false;
+              break;
+            }
+            ++vlast_uses;
+            const int first_bad = at.kv_len - t * C::KEYS;  // rows [first_bad, 128) hold no key
+            const int n16 = (C::KEYS - first_bad) * 8;      // 16-byte chunks per half
+            for (int h = 0; h < C::HALVES; ++h)
+              for (int i = lane; i < n16; i += 32)
+                *reinterpret_cast<uint4*>(vdst + h * C::KHALF + first_bad * 128 + i * 16) =
+                    make_uint4(0, 0, 0, 0);
+            tc::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bar[B_VFULL + st]);
+          }
+        }
       }
-      const bool has1 = t * C::KEYS + 64 < kv_len;
-      uint8_t* kdst = sKV + st * 2 * C::KVTILE;
-      uint8_t* vdst = kdst + C::KVTILE;
-      const bool last_partial = (t == n_kv - 1) && (kv_len % C::KEYS != 0);
-      uint64_t* vbar = last_partial ? &bar[B_VLAST] : &bar[B_VFULL + st];
+      if (!ok && lane == 0) set_dev_error(a.header, DS_DEVERR_WORKLIST);
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
       if (lane == 0) {
-        const uint32_t tx = (has1 ? 2u : 1u) * box_tx;
-        mbar_arrive_expect_tx(&bar[B_KFULL + st], tx);
-        mbar_arrive_expect_tx(vbar, tx);
-        for (int i = 0; i < (has1 ? 2 : 1); ++i) {
-          int blk = btab[2 * t + i];
-          if (blk < 0 || blk >= a.num_blocks) {
-            set_dev_error(a.header, DS_DEVERR_BLOCK_ID);
-            blk = 0;
+        constexpr uint32_t IQK = tc::idesc_f16(BF16, 128, 128, false);
+        constexpr uint32_t IPV = tc::idesc_f16(BF16, 128, D, true);
+        auto qk = [&](int x, uint32_t r) {
+          const uint32_t qa = smem_u32(sQ + x * C::QTILE);
+          const uint32_t kb = smem_u32(sKV + (r & 1) * 2 * C::KVTILE);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t oq = (ks / 4) * C::QHALF + (ks % 4) * 32;
+            const uint32_t ok_ = (ks / 4) * C::KHALF + (ks % 4) * 32;
+            tc::mma_ss(tmem + C::COL_S0 + 128 * x, tc::smem_desc_sw128(qa + oq, 16, 1024),
+                       tc::smem_desc_sw128(kb + ok_, 16, 1024), IQK, ks > 0);
           }
-          const int krow = ((blk * 2 + 0) * a.Hkv + c) * 64;
-          const int vrow = ((blk * 2 + 1) * a.Hkv + c) * 64;
+          tc::mma_commit(&bar[B_SFULL + x]);
+        };
+        auto pv = [&](int x, uint32_t r, bool acc) {
+          const uint32_t vb = smem_u32(sKV + (r & 1) * 2 * C::KVTILE + C::KVTILE);
 #pragma unroll
-          for (int h = 0; h < C::HALVES; ++h) {
-            tc::tma_load_2d(kdst + h * C::KHALF + i * C::BOX_BYTES, &pool_map, h * 64, krow,
-                            &bar[B_KFULL + st]);
-            tc::tma_load_2d(vdst + h * C::KHALF + i * C::BOX_BYTES, &pool_map, h * 64, vrow,
-                            vbar);
-          }
-        }
-      }
-      if (last_partial) {
-        if (!mbar_wait_bounded(&bar[B_VLAST], 0)) {
-          if (lane == 0) set_dev_error(a.header, DS_DEVERR_WORKLIST);
-          break;
-        }
-        const int first_bad = kv_len - t * C::KEYS;  // rows [first_bad, 128) hold no key
-        const int n16 = (C::KEYS - first_bad) * 8;   // 16-byte chunks per half
-        for (int h = 0; h < C::HALVES; ++h)
-          for (int i = lane; i < n16; i += 32)
-            *reinterpret_cast<uint4*>(vdst + h * C::KHALF + first_bad * 128 + i * 16) =
-                make_uint4(0, 0, 0, 0);
-        tc::fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bar[B_VFULL + st]);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IQK = tc::idesc_f16(BF16, 128, 128, false);
-      constexpr uint32_t IPV = tc::idesc_f16(BF16, 128, D, true);
-      bool ok = mbar_wait_bounded(&bar[B_QREADY], 0);
-      auto qk = [&](int x, int t) {
-        const uint32_t qa = smem_u32(sQ + x * C::QTILE);
-        const uint32_t kb = smem_u32(sKV + (t & 1) * 2 * C::KVTILE);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t oq = (ks / 4) * C::QHALF + (ks % 4) * 32;
-          const uint32_t ok_ = (ks / 4) * C::KHALF + (ks % 4) * 32;
-          tc::mma_ss(tmem + C::COL_S0 + 128 * x, tc::smem_desc_sw128(qa + oq, 16, 1024),
-                     tc::smem_desc_sw128(kb + ok_, 16, 1024), IQK, ks > 0);
-        }
-        tc::mma_commit(&bar[B_SFULL + x]);
-      };
-      auto pv = [&](int x, int t) {
-        const uint32_t vb = smem_u32(sKV + (t & 1) * 2 * C::KVTILE + C::KVTILE);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc::mma_ts(tmem + C::COL_O0 + D * x, tmem + C::COL_S0 + 128 * x + 8 * kk,
-                     tc::smem_desc_sw128(vb + kk * 2048, C::KHALF, 1024), IPV, (t > 0 || kk > 0));
-        tc::mma_commit(&bar[B_ODONE + x]);
-      };
-      if (ok) ok = mbar_wait_bounded(&bar[B_KFULL], 0);
-      if (ok) {
-        tc::fence_after();
-        qk(0, 0);
-        if (has_b) qk(1, 0);
-      }
-      for (int t = 0; ok && t < n_kv; ++t) {
-        const int st = t & 1;
-        ok = mbar_wait_bounded(&bar[B_VFULL + st], (t >> 1) & 1) &&
-             mbar_wait_bounded(&bar[B_PFULL + 0], t & 1);
-        if (!ok) break;
-        tc::fence_after();
-        pv(0, t);
-        if (t + 1 < n_kv) {
-          ok = mbar_wait_bounded(&bar[B_KFULL + (st ^ 1)], ((t + 1) >> 1) & 1);
+          for (int kk = 0; kk < 8; ++kk)
+            tc::mma_ts(tmem + C::COL_O0 + D * x, tmem + C::COL_S0 + 128 * x + 8 * kk,
+                       tc::smem_desc_sw128(vb + kk * 2048, C::KHALF, 1024), IPV, (acc || kk > 0));
+          tc::mma_commit(&bar[B_ODONE + x]);
+        };
+        uint32_t ring = 0, qn[2] = {0, 0}, stp[2] = {0, 0};
+        bool ok = true;
+        for (int rnd = 0, k = snake_atom(0); ok && k < n_atoms; k = snake_atom(++rnd)) {
+          Atom at;
+          if (!load_atom(k, at)) continue;
+          ok = mbar_wait_bounded(&bar[B_QREADY + 0], qn[0] & 1) &&
+               mbar_wait_bounded(&bar[B_KFULL + (ring & 1)], (ring >> 1) & 1);
+          ++qn[0];
           if (!ok) break;
           tc::fence_after();
-          qk(0, t + 1);
+          qk(0, ring);
+          if (at.has_b) {
+            ok = mbar_wait_bounded(&bar[B_QREADY + 1], qn[1] & 1);
+            ++qn[1];
+            if (!ok) break;
+            tc::fence_after();
+            qk(1, ring);
+          }
+          for (int t = 0; t < at.n_kv; ++t) {
+            const uint32_t r = ring + t;
+            ok = mbar_wait_bounded(&bar[B_VFULL + (r & 1)], (r >> 1) & 1) &&
+                 mbar_wait_bounded(&bar[B_PFULL + 0], stp[0] & 1);
+            if (!ok) break;
+            tc::fence_after();
+            pv(0, r, t > 0);
+            ++stp[0];
+            if (t + 1 < at.n_kv) {
+              ok = mbar_wait_bounded(&bar[B_KFULL + ((r + 1) & 1)], ((r + 1) >> 1) & 1);
+              if (!ok) break;
+              tc::fence_after();
+              qk(0, r + 1);
+            }
+            if (at.has_b) {
+              ok = mbar_wait_bounded(&bar[B_PFULL + 1], stp[1] & 1);
+              if (!ok) break;
+              tc::fence_after();
+              pv(1, r, t > 0);
+              ++stp[1];
+            }
+            tc::mma_commit(&bar[B_KVEMPTY + (r & 1)]);
+            if (at.has_b && t + 1 < at.n_kv) qk(1, r + 1);
+          }
+          ring += at.n_kv;
         }
-        if (has_b) {
-          ok = mbar_wait_bounded(&bar[B_PFULL + 1], t & 1);
-          if (!ok) break;
-          tc::fence_after();
-          pv(1, t);
-        }
-        tc::mma_commit(&bar[B_KVEMPTY + st]);
-        if (has_b && t + 1 < n_kv) qk(1, t + 1);
+        if (!ok) set_dev_error(a.header, DS_DEVERR_WORKLIST);
       }
-      if (!ok) set_dev_error(a.header, DS_DEVERR_WORKLIST);
+      __syncwarp();
+      // free tensor memory once every softmax thread has read its last values
+      (void)mbar_wait_bounded(&bar[B_DONE], 0);
+      __syncwarp();
+      tc::fence_after();
+      tc::tmem_dealloc(tmem, C::TMEM_COLS);
+      tc::tmem_relinquish();
     }
-    __syncwarp();
-    // free tensor memory once every softmax thread has read its last values
-    (void)mbar_wait_bounded(&bar[B_DONE], 0);
-    __syncwarp();
-    tc::fence_after();
-    tc::tmem_dealloc(tmem, C::TMEM_COLS);
-    tc::tmem_relinquish();
-  }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 208;\n" ::: "memory");
     // ------------------------------------------------------------ softmax
     const int x = (warp - 4) >> 2;            // 0: tile A, 1: tile B
     const int r = 32 * (warp & 3) + lane;     // row = tensor-memory lane
-    const int jt = x * T + r / G;             // token of this row inside the atom
-    const bool valid = jt < ntok;
-    const int head = c * G + r % G;
-    const int pos = s_seen + j0 + min(jt, ntok - 1);
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const uint32_t col_s = C::COL_S0 + 128 * x;
     const uint32_t col_o = C::COL_O0 + D * x;
+    const float sc = a.scale_log2;
+    uint32_t stp = 0;  // KV steps of tile x done by this CTA
+    bool ok = true;
+    for (int rnd = 0, k = snake_atom(0); ok && k < n_atoms; k = snake_atom(++rnd)) {
+      Atom at;
+      if (!load_atom(k, at)) continue;
+      if (x == 1 && !at.has_b) continue;
+      const int jt = x * T + r / G;             // token of this row inside the atom
+      const bool valid = jt < at.ntok;
+      const int head = at.c * G + r % G;
+      const int pos = at.s_seen + at.j0 + min(jt, at.ntok - 1);
 
-    // Q row: rotate on load, round to the storage type, 128-byte swizzle.
-    {
-      uint8_t* qt = sQ + x * C::QTILE;
-      const float4* cs4 = reinterpret_cast<const float4*>(a.rope) + (int64_t)pos * (D / 4);
-      const uint16_t* src = qkv + (int64_t)(tok0 + min(jt, ntok - 1)) * ((a.Hq + 2 * a.Hkv) * D) + head * D;
+      // Q row: rotate on load, round to the storage type, 128-byte swizzle.
+      {
+        uint8_t* qt = sQ + x * C::QTILE;
+        const float4* cs4 = reinterpret_cast<const float4*>(a.rope) + (int64_t)pos * (D / 4);
+        const uint16_t* src =
+            qkv + (int64_t)(at.tok0 + min(jt, at.ntok - 1)) * ((a.Hq + 2 * a.Hkv) * D) + head * D;
 #pragma unroll
-      for (int cc = 0; cc < D / 16; ++cc) {
-        const int ch0 = HALF ? cc : 2 * cc;
-        const int ch1 = HALF ? D / 16 + cc : 2 * cc + 1;
-        uint4 x0 = make_uint4(0, 0, 0, 0), x1 = make_uint4(0, 0, 0, 0);
-        if (valid && (x == 0 || has_b)) {
-          x0 = ld_nc_v4(src + 8 * ch0);
-          x1 = ld_nc_v4(src + 8 * ch1);
-          float4 cs[4];
+        for (int cc = 0; cc < D / 16; ++cc) {
+          const int ch0 = HALF ? cc : 2 * cc;
+          const int ch1 = HALF ? D / 16 + cc : 2 * cc + 1;
+          uint4 x0 = make_uint4(0, 0, 0, 0), x1 = make_uint4(0, 0, 0, 0);
+          if (valid) {
+            x0 = ld_nc_v4(src + 8 * ch0);
+            x1 = ld_nc_v4(src + 8 * ch1);
+            float4 cs[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) cs[q] = __ldg(cs4 + 4 * cc + q);
-          rotate16<BF16, HALF>(x0, x1, cs);
+            for (int q = 0; q < 4; ++q) cs[q] = __ldg(cs4 + 4 * cc + q);
+            rotate16<BF16, HALF>(x0, x1, cs);
+          }
+          *reinterpret_cast<uint4*>(qt + (ch0 / 8) * C::QHALF + r * 128 + (((ch0 % 8) ^ (r & 7)) << 4)) = x0;
+          *reinterpret_cast<uint4*>(qt + (ch1 / 8) * C::QHALF + r * 128 + (((ch1 % 8) ^ (r & 7)) << 4)) = x1;
         }
-        *reinterpret_cast<uint4*>(qt + (ch0 / 8) * C::QHALF + r * 128 + (((ch0 % 8) ^ (r & 7)) << 4)) = x0;
-        *reinterpret_cast<uint4*>(qt + (ch1 / 8) * C::QHALF + r * 128 + (((ch1 % 8) ^ (r & 7)) << 4)) = x1;
+        tc::fence_proxy_async();
+        tc::mbar_arrive(&bar[B_QREADY + x]);
       }
-      tc::fence_proxy_async();
-      tc::mbar_arrive(&bar[B_QREADY]);
-    }
 
-    if (x == 0 || has_b) {
       float m_ref = -INFINITY, l = 0.f;  // m_ref in log2 units (scaled)
-      const float sc = a.scale_log2;
-      bool ok = true;
-      for (int t = 0; t < n_kv; ++t) {
-        if (!mbar_wait_bounded(&bar[B_SFULL + x], t & 1)) { ok = false; break; }
+      for (int t = 0; t < at.n_kv; ++t, ++stp) {
+        if (!mbar_wait_bounded(&bar[B_SFULL + x], stp & 1)) { ok = false; break; }
         tc::fence_after();
         // the whole S row of this KV tile, one wait
         uint32_t v[128];
@@ -313,7 +361,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
           m_ref = mx;
         }
         if (t > 0) {  // P(t) overwrites P(t-1); O must hold PV(t-1) before a rescale
-          if (!mbar_wait_bounded(&bar[B_ODONE + x], (t - 1) & 1)) { ok = false; break; }
+          if (!mbar_wait_bounded(&bar[B_ODONE + x], (stp - 1) & 1)) { ok = false; break; }
           tc::fence_after();
         }
         const float nm = -m_ref;
@@ -350,30 +398,30 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
         tc::fence_before();
         tc::mbar_arrive(&bar[B_PFULL + x]);
       }
-      if (ok && mbar_wait_bounded(&bar[B_ODONE + x], (n_kv - 1) & 1)) {
-        tc::fence_after();
-        const float inv = 1.f / l;
-        uint16_t* dst = out + (int64_t)(tok0 + jt) * a.Hq * D + head * D;
+      if (!ok) break;
+      // epilogue: the atom's last P*V, then O / l -> out
+      if (!mbar_wait_bounded(&bar[B_ODONE + x], (stp - 1) & 1)) { ok = false; break; }
+      tc::fence_after();
+      const float inv = 1.f / l;
+      uint16_t* dst = out + (int64_t)(at.tok0 + jt) * a.Hq * D + head * D;
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t v[32];
-          tc::tmem_ld32(lane_addr + col_o + 32 * ch, v);
-          tc::tmem_wait_ld();
-          if (valid) {
-            uint32_t pk[16];
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        tc::tmem_ld32(lane_addr + col_o + 32 * ch, v);
+        tc::tmem_wait_ld();
+        if (valid) {
+          uint32_t pk[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              pk[e] = Stor<BF16>::pack(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+          for (int e = 0; e < 16; ++e)
+            pk[e] = Stor<BF16>::pack(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              *reinterpret_cast<uint4*>(dst + 32 * ch + 8 * q) =
-                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-          }
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(dst + 32 * ch + 8 * q) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
-      } else {
-        set_dev_error(a.header, DS_DEVERR_WORKLIST);
       }
     }
+    if (!ok) set_dev_error(a.header, DS_DEVERR_WORKLIST);
     tc::fence_before();
     tc::mbar_arrive(&bar[B_DONE]);
   }
@@ -429,8 +477,17 @@ static cudaError_t launch_prefill_t(const ds_ragged_meta& m, const LayerArgs& a,
   auto kern = prefill_tc_kernel<BF16, HALF, D, G>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(m.n_prefill_tiles, a.Hkv);
-  kern<<<grid, C::THREADS, C::SMEM, st>>>(map, reinterpret_cast<const int4*>(m.prefill_tiles),
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int n_atoms = m.n_prefill_tiles * a.Hkv;
+  // Persistent grid: as many CTAs as SMs, or, with decode rows queued behind
+  // this kernel, the SMs the prefill work needs to finish alongside them.
+  int ctas = sms;
+  if (m.prefill_sms > 0.f) ctas = (int)std::ceil(m.prefill_sms);
+  ctas = std::max(1, std::min(ctas, std::min(sms, n_atoms)));
+  kern<<<ctas, C::THREADS, C::SMEM, st>>>(map, reinterpret_cast<const int4*>(m.prefill_tiles), n_atoms,
                                           m.cu_seqlens, m.seq_seen, m.blk_off, m.block_table,
                                           static_cast<const uint16_t*>(qkv),
                                           static_cast<uint16_t*>(out), a);

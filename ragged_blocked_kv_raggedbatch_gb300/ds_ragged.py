@@ -56,7 +56,7 @@ class ds_ragged_meta(ctypes.Structure):
                 ("n_seqs", i32), ("n_tokens", i32), ("n_blocks", i32),
                 ("n_prefill_seqs", i32), ("n_decode_seqs", i32), ("n_prefill_tiles", i32),
                 ("n_decode_items", i32), ("max_len", i32), ("pool_num_blocks", i32),
-                ("split_blocks", i32), ("used_bytes", ctypes.c_size_t),
+                ("split_blocks", i32), ("prefill_sms", ctypes.c_float), ("used_bytes", ctypes.c_size_t),
                 ("header", P), ("cu_seqlens", P), ("seq_seen", P), ("seq_new", P),
                 ("blk_off", P), ("block_table", P), ("tok_seq", P), ("tok_pos", P),
                 ("prefill_tiles", P), ("decode_items", P), ("decode_seqs", P)]

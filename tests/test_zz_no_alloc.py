@@ -81,9 +81,9 @@ def test_static_workspace_matches_workspace_entry_point_two_calls():
 def test_static_workspace_rejects_oversize_batch():
     """A batch whose split partials exceed the built-in array is refused with
     DS_ERR_WORKSPACE before anything is enqueued."""
-    # 256 decode rows of 8192 keys, 32 query heads of d=128: 16 splits each,
-    # 4096 items x 32 heads x 130 floats = 68 MB > 32 MiB
-    wl = W.make_custom([(8191, 1)] * 256, 32, 32, 128, dtype="bf16", seed=3)
+    # 640 decode rows of 8192 keys, 32 query heads of d=128: 4 splits of 32
+    # blocks each, 2560 items x 32 heads x 130 floats = 42.6 MB > 32 MiB
+    wl = W.make_custom([(8191, 1)] * 640, 32, 32, 128, dtype="bf16", seed=3)
     params = R.params_for(wl)
     nb = int(wl.blocks_needed().sum())
     dev_b, stg_b = R.ds_meta_buffer_sizes(wl.n_seqs, wl.n_tokens, nb, params)
