@@ -33,6 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+from ragged_blocked_kv_raggedbatch_gb300 import replicas  # noqa: E402
 from ragged_blocked_kv_raggedbatch_gb300 import workloads as W  # noqa: E402
 
 DEFAULT_WORKLOAD = "decode256_mha_d128"
@@ -154,13 +155,6 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _dist():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
-
-
 # ----------------------------------------------------------- CPU oracle legs
 
 def _oracle_sample(wl, n_rows_target: int, seed: int = 0, max_pool_bytes: float = 256e6):
@@ -216,7 +210,7 @@ def time_oracle(wl, seconds: float = 12.0, seed: int = 0):
 
 
 def reference_arm(args, wl):
-    ws, rank, _ = _dist()
+    ws, rank, _ = replicas.env()
     if rank != 0:
         return 0
     import oracle
@@ -266,20 +260,16 @@ def gpu_arm(args, wl):
     import torch
     from ragged_blocked_kv_raggedbatch_gb300 import ds_ragged as R
 
-    ws, rank, local = _dist()
+    ws, rank, local = replicas.env()
     torch.cuda.set_device(local)
-    pg = None
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-        pg = dist
+    grp = replicas.Group("nccl")
     dev = "cuda"
     stream = torch.cuda.Stream()
     peaks = load_peaks()
     alg = algorithmic(wl)
     nb_total = int(wl.blocks_needed().sum())
     with torch.cuda.stream(stream):
-        qkv, pool = W.make_values(wl, dev, seed=wl.seed + rank)
+        qkv, pool = W.make_values(wl, dev, seed=replicas.rank_seed(wl.seed, rank))
         params = R.params_for(wl)
         layer = R.RaggedLayer(params, wl.n_seqs, wl.n_tokens, nb_total, wl.max_len(), stream=stream)
         descs = R.SeqDescs.of(wl)
@@ -308,8 +298,7 @@ def gpu_arm(args, wl):
         if flush is not None:
             flush.zero_()
     stream.synchronize()
-    if pg:
-        pg.barrier()
+    grp.barrier()
     torch.cuda.synchronize()
 
     K = args.steps
@@ -331,11 +320,7 @@ def gpu_arm(args, wl):
     step_ms = [a.elapsed_time(c) for a, b, c in ev]
     attn_ms = [b.elapsed_time(c) for a, b, c in ev]
     app_ms = [a.elapsed_time(b) for a, b, c in ev]
-    total_ms = float(sum(step_ms))
-    if pg:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = grp.max(float(sum(step_ms)), dev)
     torch.cuda.synchronize()
     ms_per_step = total_ms / K
     value = ws * wl.n_tokens * K / (total_ms / 1e3)
@@ -376,8 +361,7 @@ def gpu_arm(args, wl):
         for k in range(E + 2):
             if k == 2:
                 stream.synchronize()
-                if pg:
-                    pg.barrier()
+                grp.barrier()
                 t0 = time.perf_counter()
             with torch.cuda.stream(stream):
                 qkv.copy_(qkv_host, non_blocking=True)
@@ -385,11 +369,7 @@ def gpu_arm(args, wl):
                 step()
                 out_host.copy_(out, non_blocking=True)
             stream.synchronize()  # the result is on the host before the next step
-        e2e_s = time.perf_counter() - t0
-        if pg:
-            t = torch.tensor([e2e_s], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = grp.max(time.perf_counter() - t0, dev)
         e2e = {"value": ws * wl.n_tokens * E / e2e_s, "unit": "tokens/s",
                "h2d_bytes_per_step": int(qkv.numel() * qkv.element_size() + m.used_bytes),
                "d2h_bytes_per_step": int(out.numel() * out.element_size()), "steps": E}
@@ -421,9 +401,7 @@ def gpu_arm(args, wl):
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
-    if pg:
-        pg.barrier()
-        pg.destroy_process_group()
+    grp.close()
     return 0
 
 
