@@ -277,6 +277,41 @@ ds_status ds_blocked_attention_static_ws(const ds_ragged_meta* meta, const ds_at
  * *meta (0 = none; DS_DEVERR_* bits otherwise). */
 ds_status ds_get_device_error(const ds_ragged_meta* meta, int32_t* err, void* stream);
 
+/* ------------------------------------------------------------ block ledger -- */
+
+/* Host-side ledger of KV-pool block ids (the BlockedAllocator of "DeepSpeed
+ * Inference v2", pyshine.com/deepspeed-2, section "The front desk": allocate
+ * hands out free indices, free takes them back; the allocator is the whole
+ * memory manager, so running out or freeing an id twice is an error, never
+ * hidden).  HOST memory only; no CUDA call.  The caller owns both arrays:
+ * stack[num_blocks] (free ids) and state[num_blocks] (1 = in use). */
+typedef struct ds_block_allocator {
+    int32_t* stack;
+    uint8_t* state;
+    int32_t num_blocks;
+    int32_t n_free;
+} ds_block_allocator;
+
+/* All blocks free.  initial_order (num_blocks ids, a permutation; NULL = 0, 1,
+ * ...) is the order in which allocate hands them out.  DS_ERR_INVALID_ARG on
+ * NULL arrays or a non-permutation. */
+ds_status ds_block_allocator_init(ds_block_allocator* a, int32_t* stack, uint8_t* state,
+                                  int32_t num_blocks, const int32_t* initial_order);
+
+/* Take n free ids into out[n] (DS_ERR_CAPACITY, nothing taken, if fewer than n
+ * are free). */
+ds_status ds_block_allocator_allocate(ds_block_allocator* a, int32_t n, int32_t* out);
+
+/* Return n ids.  DS_ERR_BAD_BLOCK (nothing returned) if an id is outside the
+ * pool, not in use, or listed twice. */
+ds_status ds_block_allocator_free(ds_block_allocator* a, const int32_t* ids, int32_t n);
+
+/* Extra blocks a sequence that owns `owned` blocks needs before `new_tokens`
+ * more tokens are appended after `seen_tokens` (get_kv_requirements /
+ * extend_kv_cache of the pages): max(0, ceil((seen+new)/block_size) - owned). */
+ds_status ds_kv_blocks_required(int32_t seen_tokens, int32_t new_tokens, int32_t owned,
+                                int32_t block_size, int32_t* extra);
+
 /* Library version string. */
 const char* ds_version(void);
 

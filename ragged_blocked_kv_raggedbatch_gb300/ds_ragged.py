@@ -62,6 +62,10 @@ class ds_ragged_meta(ctypes.Structure):
                 ("prefill_tiles", P), ("decode_items", P), ("decode_seqs", P)]
 
 
+class ds_block_allocator(ctypes.Structure):
+    _fields_ = [("stack", P), ("state", P), ("num_blocks", i32), ("n_free", i32)]
+
+
 # name -> (restype, argtypes); every entry point of include/ds_ragged.h
 SIGNATURES = {
     "ds_last_error": (ctypes.c_char_p, []),
@@ -76,6 +80,10 @@ SIGNATURES = {
     "ds_blocked_attention": (i32, [P, P, P, P, P, P, P, ctypes.c_size_t, P]),
     "ds_get_device_error": (i32, [P, P, P]),
     "ds_blocked_attention_static_ws": (i32, [P, P, P, P, P, P, P]),
+    "ds_block_allocator_init": (i32, [P, P, P, i32, P]),
+    "ds_block_allocator_allocate": (i32, [P, i32, P]),
+    "ds_block_allocator_free": (i32, [P, P, i32]),
+    "ds_kv_blocks_required": (i32, [i32, i32, i32, i32, P]),
 }
 
 DS_STATIC_WORKSPACE_BYTES = 32 << 20
@@ -232,6 +240,40 @@ def ds_get_device_error(meta: ds_ragged_meta, stream=None) -> int:
     v = ctypes.c_int32(0)
     _check(load().ds_get_device_error(_ref(meta), _ref(v), _stream(stream)), "ds_get_device_error")
     return v.value
+
+
+class BlockAllocator:
+    """The C-ABI block ledger with its two host arrays."""
+
+    def __init__(self, num_blocks: int, initial_order=None):
+        self.stack = np.zeros(max(num_blocks, 1), np.int32)
+        self.state = np.zeros(max(num_blocks, 1), np.uint8)
+        self.a = ds_block_allocator()
+        order = None if initial_order is None else np.ascontiguousarray(initial_order, np.int32)
+        self._order = order
+        _check(load().ds_block_allocator_init(_ref(self.a), self.stack.ctypes.data, self.state.ctypes.data,
+                                              num_blocks, None if order is None else order.ctypes.data),
+               "ds_block_allocator_init")
+
+    @property
+    def n_free(self) -> int:
+        return self.a.n_free
+
+    def allocate(self, n: int) -> np.ndarray:
+        out = np.zeros(max(n, 1), np.int32)
+        _check(load().ds_block_allocator_allocate(_ref(self.a), n, out.ctypes.data), "ds_block_allocator_allocate")
+        return out[:n].copy()
+
+    def free(self, ids) -> None:
+        ids = np.ascontiguousarray(ids, np.int32)
+        _check(load().ds_block_allocator_free(_ref(self.a), ids.ctypes.data if len(ids) else None, len(ids)),
+               "ds_block_allocator_free")
+
+
+def ds_kv_blocks_required(seen: int, new: int, owned: int, block_size: int = 64) -> int:
+    e = ctypes.c_int32(0)
+    _check(load().ds_kv_blocks_required(seen, new, owned, block_size, _ref(e)), "ds_kv_blocks_required")
+    return e.value
 
 
 # ------------------------------------------------------- buffer management --
