@@ -405,6 +405,130 @@ def gpu_arm(args, wl):
     return 0
 
 
+# -------------------------------------------------------- component lines
+
+def _line(metric, value, unit, config, **extra):
+    d = {"metric": metric, "value": value, "unit": unit, "n_gpus": 1, "higher_is_better": True,
+         "data": "synthetic", "config": config}
+    d.update(extra)
+    print(json.dumps(d), flush=True)
+
+
+def component_offload(args, wl):
+    """BlockedKVCache offload + restore of scattered blocks between the pool
+    and page-locked host memory (one kernel each way, per 1000 blocks)."""
+    import torch
+    from ragged_blocked_kv_raggedbatch_gb300 import ds_ragged as R
+    params = R.params_for(wl)
+    nblk = min(wl.num_blocks, 4096)
+    dt = W.torch_dtype(wl)
+    pool = torch.randn((nblk, 2, wl.n_kv_heads, 64, wl.head_dim), device="cuda").to(dt)
+    bb = R.ds_kv_block_bytes(params)
+    n = min(nblk, max(1, int(2e9 // bb)))
+    ids = np.random.default_rng(0).permutation(nblk)[:n].astype(np.int32)
+    host = torch.empty((n, bb // 2), dtype=dt).pin_memory()
+    pk = R.ds_kv_pool(pool.data_ptr(), nblk)
+    st = torch.cuda.current_stream()
+    res = {}
+    for name, fn in (("offload", R.ds_kv_offload), ("restore", R.ds_kv_restore)):
+        for _ in range(args.warmup):
+            fn(params, pk, ids, host)
+        st.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(args.steps):
+            fn(params, pk, ids, host)
+        b.record(st)
+        st.synchronize()
+        res[name] = n * bb * args.steps / (a.elapsed_time(b) / 1e3) / 1e9
+    _line("kv block offload+restore GB/s", 2.0 / (1 / res["offload"] + 1 / res["restore"]), "GB/s",
+          {"workload": wl.name, "blocks": int(n), "block_bytes": int(bb), "component": "offload"},
+          offload_gbs=res["offload"], restore_gbs=res["restore"], steps=args.steps, warmup=args.warmup)
+
+
+def component_gather(args, wl):
+    """Ragged embedding gather (vocab 128k x hidden 4096, bf16) for the
+    batch's packed tokens, and the last-token logits gather."""
+    import torch
+    from ragged_blocked_kv_raggedbatch_gb300 import ds_ragged as R
+    layer = R.RaggedLayer(R.params_for(wl), wl.n_seqs, wl.n_tokens, int(wl.blocks_needed().sum()),
+                          wl.max_len())
+    layer.build(R.SeqDescs.of(wl), wl.num_blocks)
+    vocab, hidden = 131072, 4096
+    table = torch.randn((vocab, hidden), device="cuda").bfloat16()
+    ids = torch.randint(0, vocab, (wl.n_tokens,), device="cuda", dtype=torch.int32)
+    out = torch.empty((wl.n_tokens, hidden), device="cuda").bfloat16()
+    lg = torch.empty((wl.n_seqs, hidden), device="cuda").bfloat16()
+    st = torch.cuda.current_stream()
+    t = {}
+    for name, fn in (("embedding", lambda: R.ds_ragged_embedding(layer.meta, ids, table, out)),
+                     ("logits", lambda: R.ds_ragged_logits_gather(layer.meta, out, lg))):
+        for _ in range(args.warmup):
+            fn()
+        st.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(args.steps):
+            fn()
+        b.record(st)
+        st.synchronize()
+        t[name] = a.elapsed_time(b) / args.steps / 1e3
+    emb_bytes = 2 * wl.n_tokens * hidden * 2
+    _line("ragged embedding gather GB/s", emb_bytes / t["embedding"] / 1e9, "GB/s",
+          {"workload": wl.name, "vocab": vocab, "hidden": hidden, "component": "gather"},
+          embedding_us=t["embedding"] * 1e6, logits_gather_us=t["logits"] * 1e6,
+          logits_gather_gbs=2 * wl.n_seqs * hidden * 2 / t["logits"] / 1e9)
+
+
+def component_multistep(args, wl):
+    """A Dynamic SplitFuse run: 256 requests (prompts log-uniform 32..2048,
+    16..256 generated tokens each) through the block ledger, the planner and
+    the layer, pass after pass; the workload's head shape, token budget 8192."""
+    import torch
+    from ragged_blocked_kv_raggedbatch_gb300 import ds_ragged as R
+    from ragged_blocked_kv_raggedbatch_gb300.splitfuse import SplitFusePlanner
+    rng = np.random.default_rng(args.seed)
+    prompts = np.floor(np.exp(rng.uniform(np.log(32), np.log(2048), 256))).astype(int)
+    gens = rng.integers(16, 256, 256, endpoint=True)
+    nblk = int(sum(-(-(p + g) // 64) for p, g in zip(prompts, gens))) + 64
+    params = R.params_for(wl)
+    alloc = R.BlockAllocator(nblk, rng.permutation(nblk))
+    plan = SplitFusePlanner(alloc, 8192, 256)
+    for i in range(256):
+        plan.add(i, int(prompts[i]), int(gens[i]))
+    dt = W.torch_dtype(wl)
+    pool = torch.randn((nblk, 2, wl.n_kv_heads, 64, wl.head_dim), device="cuda").to(dt)
+    qkv = torch.randn((8192, wl.qkv_width), device="cuda").to(dt)
+    out = torch.empty((8192, wl.n_q_heads * wl.head_dim), device="cuda").to(dt)
+    st = torch.cuda.Stream()
+    layer = R.RaggedLayer(params, 256, 8192, nblk, 4096, stream=st)
+    evs, host_s, toks, passes = [], 0.0, 0, 0
+    torch.cuda.synchronize()
+    while not plan.idle:
+        t0 = time.perf_counter()
+        batch = plan.next_batch()
+        descs = R.SeqDescs([b[1] for b in batch], [b[2] for b in batch], [b[3] for b in batch])
+        with torch.cuda.stream(st):
+            layer.build(descs, nblk)
+            host_s += time.perf_counter() - t0
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            layer.append(qkv, pool)
+            layer.attention(qkv, pool, out)
+            b.record(st)
+        evs.append((a, b))
+        n = sum(x[2] for x in batch)
+        toks += n
+        passes += 1
+        st.synchronize()  # the staging buffer is reused by the next pass
+        plan.commit(batch)
+    dev_s = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+    _line("splitfuse multi-pass new tokens/s per layer", toks / dev_s, "tokens/s",
+          {"workload": wl.name + "_heads", "requests": 256, "token_budget": 8192, "component": "multistep"},
+          passes=passes, tokens=toks, device_ms_per_pass=1e3 * dev_s / passes,
+          host_us_per_pass=1e6 * host_s / passes, layer_launches=passes * 4)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -420,6 +544,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--component", choices=["offload", "gather", "multistep"], default=None,
+                    help="measure a component next to the layer instead of the layer step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -431,6 +557,9 @@ def main(argv=None):
         wl = W.first_sequences(wl, args.subset, args.seed)
     if args.impl == "reference":
         return reference_arm(args, wl)
+    if args.component:
+        return {"offload": component_offload, "gather": component_gather,
+                "multistep": component_multistep}[args.component](args, wl) or 0
     return gpu_arm(args, wl)
 
 

@@ -57,6 +57,7 @@ typedef int32_t ds_status;
 #define DS_DEVERR_BLOCK_ID 1  /* a kernel met a block id outside the pool     */
 #define DS_DEVERR_POSITION 2  /* a position beyond the rotary table or blocks */
 #define DS_DEVERR_WORKLIST 4  /* an inconsistent work-list entry              */
+#define DS_DEVERR_TOKEN 8     /* a token id outside the embedding table       */
 
 #define DS_FP16 0
 #define DS_BF16 1
@@ -276,6 +277,49 @@ ds_status ds_blocked_attention_static_ws(const ds_ragged_meta* meta, const ds_at
 /* Wait for `stream` and read the device error word of the last batch built in
  * *meta (0 = none; DS_DEVERR_* bits otherwise). */
 ds_status ds_get_device_error(const ds_ragged_meta* meta, int32_t* err, void* stream);
+
+/* ------------------------------------------------- KV offload / restore -- */
+
+/* BlockedKVCache offload and restore ("DeepSpeed Inference v2",
+ * pyshine.com/deepspeed-2, section "The front desk": offload copies chosen
+ * blocks to host memory to free device room, restore brings them back when
+ * their sequence is rescheduled).  One block = all of its K and V tiles,
+ * 2*n_kv_heads*block_size*head_dim storage elements, contiguous in the pool. */
+ds_status ds_kv_block_bytes(const ds_attn_params* params, size_t* bytes);
+
+/* Copy pool blocks block_ids[0..n) (HOST array, read during the call) into
+ * host_dst[i*block_bytes ...] with one kernel per 1000 blocks that writes the
+ * page-locked host buffer directly (no staging copy).  host_dst: page-locked
+ * (pinned) host memory the device can address, n*block_bytes, 16-byte aligned;
+ * DS_ERR_INVALID_ARG otherwise.  Ids outside the pool: DS_ERR_BAD_BLOCK before
+ * anything is enqueued. */
+ds_status ds_kv_offload(const ds_attn_params* params, const ds_kv_pool* pool,
+                        const int32_t* block_ids, int32_t n, void* host_dst, void* stream);
+
+/* The reverse: host_src[i*block_bytes ...] -> pool block block_ids[i].  An id
+ * listed twice is DS_ERR_BAD_BLOCK (two sources for one block). */
+ds_status ds_kv_restore(const ds_attn_params* params, const ds_kv_pool* pool,
+                        const int32_t* block_ids, int32_t n, const void* host_src, void* stream);
+
+/* ----------------------------------------- ragged embedding / logits rows -- */
+
+/* RaggedEmbeddingKernel of the pages ("DeepSpeed Inference v2", section
+ * "Ragged batches"): out[t] = table[token_ids[t]] for the batch's packed tokens
+ * t < meta->n_tokens.  token_ids: DEVICE int32 [n_tokens]; table: DEVICE
+ * [vocab][hidden]; out: DEVICE [n_tokens][hidden]; elements of elem_bytes (2 or
+ * 4) bytes; hidden*elem_bytes a multiple of 16 and the pointers 16-byte
+ * aligned (DS_ERR_UNSUPPORTED / DS_ERR_INVALID_ARG otherwise).  An id outside
+ * [0, vocab) sets DS_DEVERR_TOKEN and writes a zero row. */
+ds_status ds_ragged_embedding(const ds_ragged_meta* meta, const int32_t* token_ids,
+                              const void* table, int32_t vocab, int32_t hidden, int32_t elem_bytes,
+                              void* out, void* stream);
+
+/* RaggedLogitsGather of the pages: out[i] = hidden_states[last packed token of
+ * sequence i] (cu_seqlens[i+1] - 1) for i < meta->n_seqs.  hidden_states:
+ * DEVICE [n_tokens][hidden]; out: DEVICE [n_seqs][hidden]; same element and
+ * alignment rules as ds_ragged_embedding. */
+ds_status ds_ragged_logits_gather(const ds_ragged_meta* meta, const void* hidden_states,
+                                  int32_t hidden, int32_t elem_bytes, void* out, void* stream);
 
 /* ------------------------------------------------------------ block ledger -- */
 

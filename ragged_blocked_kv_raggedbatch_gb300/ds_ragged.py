@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libds_ragged.so")
 
 DS_OK, DS_ERR_INVALID_ARG, DS_ERR_CAPACITY, DS_ERR_BAD_BLOCK = 0, 1, 2, 3
 DS_ERR_UNSUPPORTED, DS_ERR_WORKSPACE, DS_ERR_CUDA = 4, 5, 6
-DS_DEVERR_BLOCK_ID, DS_DEVERR_POSITION, DS_DEVERR_WORKLIST = 1, 2, 4
+DS_DEVERR_BLOCK_ID, DS_DEVERR_POSITION, DS_DEVERR_WORKLIST, DS_DEVERR_TOKEN = 1, 2, 4, 8
 DS_FP16, DS_BF16 = 0, 1
 DS_ROPE_HALF, DS_ROPE_INTERLEAVED = 0, 1
 STATUS_NAMES = {0: "DS_OK", 1: "DS_ERR_INVALID_ARG", 2: "DS_ERR_CAPACITY", 3: "DS_ERR_BAD_BLOCK",
@@ -84,6 +84,11 @@ SIGNATURES = {
     "ds_block_allocator_allocate": (i32, [P, i32, P]),
     "ds_block_allocator_free": (i32, [P, P, i32]),
     "ds_kv_blocks_required": (i32, [i32, i32, i32, i32, P]),
+    "ds_kv_block_bytes": (i32, [P, P]),
+    "ds_kv_offload": (i32, [P, P, P, i32, P, P]),
+    "ds_kv_restore": (i32, [P, P, P, i32, P, P]),
+    "ds_ragged_embedding": (i32, [P, P, P, i32, i32, i32, P, P]),
+    "ds_ragged_logits_gather": (i32, [P, P, i32, i32, P, P]),
 }
 
 DS_STATIC_WORKSPACE_BYTES = 32 << 20
@@ -234,6 +239,37 @@ def ds_blocked_attention_static_ws(meta: ds_ragged_meta, params: ds_attn_params,
     _check(load().ds_blocked_attention_static_ws(_ref(meta), _ref(params), _ref(rope), _ptr(qkv),
                                                  _ref(pool), _ptr(out), _stream(stream)),
            "ds_blocked_attention_static_ws")
+
+
+def ds_kv_block_bytes(params: ds_attn_params) -> int:
+    b = ctypes.c_size_t(0)
+    _check(load().ds_kv_block_bytes(_ref(params), _ref(b)), "ds_kv_block_bytes")
+    return b.value
+
+
+def ds_kv_offload(params: ds_attn_params, pool: ds_kv_pool, block_ids, host_dst, stream=None):
+    ids = np.ascontiguousarray(block_ids, np.int32)
+    _check(load().ds_kv_offload(_ref(params), _ref(pool), ids.ctypes.data if len(ids) else None, len(ids),
+                                _ptr(host_dst), _stream(stream)), "ds_kv_offload")
+
+
+def ds_kv_restore(params: ds_attn_params, pool: ds_kv_pool, block_ids, host_src, stream=None):
+    ids = np.ascontiguousarray(block_ids, np.int32)
+    _check(load().ds_kv_restore(_ref(params), _ref(pool), ids.ctypes.data if len(ids) else None, len(ids),
+                                _ptr(host_src), _stream(stream)), "ds_kv_restore")
+
+
+def ds_ragged_embedding(meta: ds_ragged_meta, token_ids, table, out, stream=None):
+    vocab, hidden = table.shape
+    _check(load().ds_ragged_embedding(_ref(meta), _ptr(token_ids), _ptr(table), vocab, hidden,
+                                      table.element_size(), _ptr(out), _stream(stream)), "ds_ragged_embedding")
+
+
+def ds_ragged_logits_gather(meta: ds_ragged_meta, hidden_states, out, stream=None):
+    hidden = hidden_states.shape[1]
+    _check(load().ds_ragged_logits_gather(_ref(meta), _ptr(hidden_states), hidden,
+                                          hidden_states.element_size(), _ptr(out), _stream(stream)),
+           "ds_ragged_logits_gather")
 
 
 def ds_get_device_error(meta: ds_ragged_meta, stream=None) -> int:

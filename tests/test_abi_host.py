@@ -237,3 +237,31 @@ def test_call_validation_before_launch(lib):
     assert attn(ws_bytes=16) == R.DS_ERR_WORKSPACE
     assert attn(ws=FAKE_DEV + 64) == R.DS_ERR_INVALID_ARG
     assert lib.ds_kv_rotary_append(None, R._ref(p), R._ref(rope), FAKE_DEV, None, R._ref(pool), None) == R.DS_ERR_INVALID_ARG
+
+
+def test_offload_restore_and_gather_validation(lib):
+    """Argument errors of the data-movement calls are found on the host."""
+    p = R.make_params(8, 2, 128)
+    bb = ctypes.c_size_t()
+    assert lib.ds_kv_block_bytes(R._ref(p), R._ref(bb)) == R.DS_OK and bb.value == 2 * 2 * 64 * 128 * 2
+    pool = R.ds_kv_pool(FAKE_DEV, 10)
+    host = np.zeros(4096, np.uint8)
+    ids = lambda *v: np.array(v, np.int32)
+    for fn in (lib.ds_kv_offload, lib.ds_kv_restore):
+        bad = ids(3, 10)
+        assert fn(R._ref(p), R._ref(pool), bad.ctypes.data, 2, host.ctypes.data, None) == R.DS_ERR_BAD_BLOCK
+        neg = ids(-1)
+        assert fn(R._ref(p), R._ref(pool), neg.ctypes.data, 1, host.ctypes.data, None) == R.DS_ERR_BAD_BLOCK
+        assert fn(R._ref(p), R._ref(pool), None, 1, host.ctypes.data, None) == R.DS_ERR_INVALID_ARG
+        assert fn(R._ref(p), R._ref(pool), None, 0, None, None) == R.DS_OK
+    dup = ids(4, 4)
+    assert lib.ds_kv_restore(R._ref(p), R._ref(pool), dup.ctypes.data, 2, host.ctypes.data, None) == R.DS_ERR_BAD_BLOCK
+    wl = W.make_custom([(5, 3), (70, 1)], 4, 2, 64)
+    pk = Packed(wl)
+    assert pk.pack() == R.DS_OK
+    tok = FAKE_DEV
+    assert lib.ds_ragged_embedding(R._ref(pk.meta), tok, FAKE_DEV, 100, 12, 2, FAKE_DEV, None) == R.DS_ERR_UNSUPPORTED
+    assert lib.ds_ragged_embedding(R._ref(pk.meta), tok, FAKE_DEV + 8, 100, 64, 2, FAKE_DEV, None) == R.DS_ERR_INVALID_ARG
+    assert lib.ds_ragged_embedding(R._ref(pk.meta), None, FAKE_DEV, 100, 64, 2, FAKE_DEV, None) == R.DS_ERR_INVALID_ARG
+    assert lib.ds_ragged_logits_gather(R._ref(pk.meta), FAKE_DEV, 64, 3, FAKE_DEV, None) == R.DS_ERR_UNSUPPORTED
+    assert lib.ds_ragged_logits_gather(None, FAKE_DEV, 64, 2, FAKE_DEV, None) == R.DS_ERR_INVALID_ARG
