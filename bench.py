@@ -529,6 +529,51 @@ def component_multistep(args, wl):
           host_us_per_pass=1e6 * host_s / passes, layer_launches=passes * 4)
 
 
+def component_graph(args, wl):
+    """One layer step (metadata upload + KV append + attention) replayed from
+    a CUDA graph vs. issued call by call, same batch."""
+    import torch
+    from ragged_blocked_kv_raggedbatch_gb300 import ds_ragged as R
+    qkv, pool = W.make_values(wl, "cuda")
+    nb = int(wl.blocks_needed().sum())
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        layer = R.RaggedLayer(R.params_for(wl), wl.n_seqs, wl.n_tokens, nb, wl.max_len(), stream=st)
+        descs = R.SeqDescs.of(wl)
+        out = torch.empty((wl.n_tokens, wl.n_q_heads * wl.head_dim), dtype=qkv.dtype, device="cuda")
+
+    def eager():
+        layer.build(descs, wl.num_blocks)
+        layer.append(qkv, pool)
+        layer.attention(qkv, pool, out)
+
+    with torch.cuda.stream(st):
+        for _ in range(args.warmup):
+            eager()
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        eager()
+    res = {}
+    for name, fn in (("eager", eager), ("graph", g.replay)):
+        with torch.cuda.stream(st):
+            for _ in range(args.warmup):
+                fn()
+            st.synchronize()
+            t0 = time.perf_counter()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            for _ in range(args.steps):
+                fn()
+            b.record(st)
+            st.synchronize()
+            res[name] = (a.elapsed_time(b) / args.steps, 1e3 * (time.perf_counter() - t0) / args.steps)
+    _line("ragged attn layer step, CUDA graph replay (new tokens/s)", wl.n_tokens / (res["graph"][1] / 1e3),
+          "tokens/s", {"workload": wl.name, "component": "graph"},
+          eager_device_ms=res["eager"][0], eager_wall_ms=res["eager"][1],
+          graph_device_ms=res["graph"][0], graph_wall_ms=res["graph"][1], steps=args.steps)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -544,7 +589,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--component", choices=["offload", "gather", "multistep"], default=None,
+    ap.add_argument("--component", choices=["offload", "gather", "multistep", "graph"], default=None,
                     help="measure a component next to the layer instead of the layer step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -559,7 +604,7 @@ def main(argv=None):
         return reference_arm(args, wl)
     if args.component:
         return {"offload": component_offload, "gather": component_gather,
-                "multistep": component_multistep}[args.component](args, wl) or 0
+                "multistep": component_multistep, "graph": component_graph}[args.component](args, wl) or 0
     return gpu_arm(args, wl)
 
 
