@@ -50,7 +50,7 @@ NCU_TRAFFIC = {
     # scaled to the full batch by its algorithmic bytes (the KV read dominates
     # and grows in proportion).
     "decode256_mha_d128": {"bytes": 9.378e9, "files": ["decode.cu", "common.cuh", "tc.cuh"],
-                           "src": "9e41ba3be6ab8e7e"},
+                           "src": "d957cf9b6883d1cc"},
 }
 
 

@@ -8,7 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/ds_ragged.h"
+#include "ds_ragged.h"
 
 namespace dsr {
 
