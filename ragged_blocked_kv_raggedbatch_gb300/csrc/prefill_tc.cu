@@ -14,10 +14,14 @@
 // Roles (12 warps = 3 warpgroups; launched at 168 registers a thread, the
 // first warpgroup gives registers back (setmaxnreg 80) and the two softmax
 // warpgroups take them (setmaxnreg 208): 128*80 + 2*128*208 <= 384*168):
-//   warp 0      TMA producer: K/V tiles into a 2-stage ring (one KV tile ahead);
-//               zeroes the rows of the final V tile past the chunk's last key
-//               (those slots may hold anything and 0 * NaN would poison P*V).
-//   warp 1      tensor-memory owner and MMA issuer (one thread):
+//   warp 0      TMA producer: K and V tiles into 2-stage rings whose slots are
+//               freed separately (K after the last QK MMA that reads it, V after
+//               the last PV MMA), so each K tile is requested about a step and a
+//               half before its first QK; zeroes the rows of the final V tile
+//               past the chunk's last key (those slots may hold anything and
+//               0 * NaN would poison P*V).
+//   warp 1      tensor-memory owner and MMA issuer (the warp walks the schedule
+//               and builds warp-uniform descriptors; one elected lane issues):
 //                 S_X = Q_X K_t^T   (SS MMA, 128 x 128 x D)
 //                 O_X += P_X V_t    (TS MMA: P read from tensor memory)
 //               issued as QK_A(0) QK_B(0) | PV_A(t) QK_A(t+1) PV_B(t) QK_B(t+1) ...
@@ -59,9 +63,12 @@ struct PfCfg {
   static constexpr int THREADS = 384;
 };
 
+// K and V slots of a ring stage are released separately: K once the last
+// QK MMA of its step has read it, V once the last PV MMA has, so the next K
+// tile is requested a whole step before it is needed.
 enum {
-  B_QREADY = 0, B_KFULL = 2, B_VFULL = 4, B_KVEMPTY = 6, B_SFULL = 8, B_PFULL = 10,
-  B_ODONE = 12, B_VLAST = 14, B_DONE = 15, B_COUNT = 16
+  B_QREADY = 0, B_KFULL = 2, B_VFULL = 4, B_KEMPTY = 6, B_SFULL = 8, B_PFULL = 10,
+  B_ODONE = 12, B_VLAST = 14, B_DONE = 15, B_VEMPTY = 16, B_COUNT = 18
 };
 
 template <bool BF16, bool HALF, int D, int G>
@@ -89,7 +96,8 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
       mbar_init(&bar[B_QREADY + s], 128);
       mbar_init(&bar[B_KFULL + s], 1);
       mbar_init(&bar[B_VFULL + s], 1);
-      mbar_init(&bar[B_KVEMPTY + s], 1);
+      mbar_init(&bar[B_KEMPTY + s], 1);
+      mbar_init(&bar[B_VEMPTY + s], 1);
       mbar_init(&bar[B_SFULL + s], 1);
       mbar_init(&bar[B_PFULL + s], 128);
       mbar_init(&bar[B_ODONE + s], 1);
@@ -151,33 +159,48 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
         if (!load_atom(k, at)) continue;
         for (int t = 0; t < at.n_kv; ++t, ++ring) {
           const int st = ring & 1;
-          if (ring >= 2 && !mbar_wait_bounded(&bar[B_KVEMPTY + st], ((ring >> 1) - 1) & 1)) {
-            ok = false;
-            break;
-          }
+          const uint32_t empty_par = ((ring >> 1) - 1) & 1;
           const bool has1 = t * C::KEYS + 64 < at.kv_len;
           uint8_t* kdst = sKV + st * 2 * C::KVTILE;
           uint8_t* vdst = kdst + C::KVTILE;
           const bool last_partial = (t == at.n_kv - 1) && (at.kv_len % C::KEYS != 0);
           uint64_t* vbar = last_partial ? &bar[B_VLAST] : &bar[B_VFULL + st];
+          int blk[2] = {0, 0};
+          for (int i = 0; i < (has1 ? 2 : 1); ++i) {
+            blk[i] = at.btab[2 * t + i];
+            if (blk[i] < 0 || blk[i] >= a.num_blocks) {
+              if (lane == 0) set_dev_error(a.header, DS_DEVERR_BLOCK_ID);
+              blk[i] = 0;
+            }
+          }
+          const uint32_t tx = (has1 ? 2u : 1u) * box_tx;
+          // K slot free (the QK MMAs of ring step ring-2 are done)
+          if (ring >= 2 && !mbar_wait_bounded(&bar[B_KEMPTY + st], empty_par)) {
+            ok = false;
+            break;
+          }
           if (lane == 0) {
-            const uint32_t tx = (has1 ? 2u : 1u) * box_tx;
             mbar_arrive_expect_tx(&bar[B_KFULL + st], tx);
-            mbar_arrive_expect_tx(vbar, tx);
             for (int i = 0; i < (has1 ? 2 : 1); ++i) {
-              int blk = at.btab[2 * t + i];
-              if (blk < 0 || blk >= a.num_blocks) {
-                set_dev_error(a.header, DS_DEVERR_BLOCK_ID);
-                blk = 0;
-              }
-              const int krow = ((blk * 2 + 0) * a.Hkv + at.c) * 64;
-              const int vrow = ((blk * 2 + 1) * a.Hkv + at.c) * 64;
+              const int krow = ((blk[i] * 2 + 0) * a.Hkv + at.c) * 64;
 #pragma unroll
-              for (int h = 0; h < C::HALVES; ++h) {
+              for (int h = 0; h < C::HALVES; ++h)
                 tc::tma_load_2d(kdst + h * C::KHALF + i * C::BOX_BYTES, &pool_map, h * 64, krow,
                                 &bar[B_KFULL + st]);
+            }
+          }
+          // V slot free (the PV MMAs of ring step ring-2 are done)
+          if (ring >= 2 && !mbar_wait_bounded(&bar[B_VEMPTY + st], empty_par)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(vbar, tx);
+            for (int i = 0; i < (has1 ? 2 : 1); ++i) {
+              const int vrow = ((blk[i] * 2 + 1) * a.Hkv + at.c) * 64;
+#pragma unroll
+              for (int h = 0; h < C::HALVES; ++h)
                 tc::tma_load_2d(vdst + h * C::KHALF + i * C::BOX_BYTES, &pool_map, h * 64, vrow, vbar);
-              }
             }
           }
           if (last_partial) {
@@ -201,74 +224,94 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
       if (!ok && lane == 0) set_dev_error(a.header, DS_DEVERR_WORKLIST);
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
-      if (lane == 0) {
+      // The whole warp walks the schedule, waits on the barriers and builds the
+      // operand descriptors (warp-uniform values); one elected lane issues each
+      // group of MMAs and every commit, so all commits track its MMAs.
+      {
         constexpr uint32_t IQK = tc::idesc_f16(BF16, 128, 128, false);
         constexpr uint32_t IPV = tc::idesc_f16(BF16, 128, D, true);
+        auto wait = [&](int b, uint32_t parity) -> bool {
+          return __all_sync(0xffffffffu, mbar_wait_bounded(&bar[b], parity));
+        };
+        auto commit = [&](int b) {
+          if (tc::elect_one()) tc::mma_commit(&bar[b]);
+          __syncwarp();
+        };
+        // descriptor start-address field = byte address / 16 (addresses stay
+        // below 256 KB, so adding an offset / 16 never carries out of it)
         auto qk = [&](int x, uint32_t r) {
-          const uint32_t qa = smem_u32(sQ + x * C::QTILE);
-          const uint32_t kb = smem_u32(sKV + (r & 1) * 2 * C::KVTILE);
+          const uint64_t qd = tc::smem_desc_sw128(smem_u32(sQ + x * C::QTILE), 16, 1024);
+          const uint64_t kd = tc::smem_desc_sw128(smem_u32(sKV + (r & 1) * 2 * C::KVTILE), 16, 1024);
+          if (tc::elect_one()) {
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t oq = (ks / 4) * C::QHALF + (ks % 4) * 32;
-            const uint32_t ok_ = (ks / 4) * C::KHALF + (ks % 4) * 32;
-            tc::mma_ss(tmem + C::COL_S0 + 128 * x, tc::smem_desc_sw128(qa + oq, 16, 1024),
-                       tc::smem_desc_sw128(kb + ok_, 16, 1024), IQK, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t oq = ((ks / 4) * C::QHALF + (ks % 4) * 32) >> 4;
+              const uint32_t ok_ = ((ks / 4) * C::KHALF + (ks % 4) * 32) >> 4;
+              tc::mma_ss(tmem + C::COL_S0 + 128 * x, qd + oq, kd + ok_, IQK, ks > 0);
+            }
+            tc::mma_commit(&bar[B_SFULL + x]);
           }
-          tc::mma_commit(&bar[B_SFULL + x]);
+          __syncwarp();
         };
         auto pv = [&](int x, uint32_t r, bool acc) {
-          const uint32_t vb = smem_u32(sKV + (r & 1) * 2 * C::KVTILE + C::KVTILE);
+          const uint64_t vd =
+              tc::smem_desc_sw128(smem_u32(sKV + (r & 1) * 2 * C::KVTILE + C::KVTILE), C::KHALF, 1024);
+          if (tc::elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            tc::mma_ts(tmem + C::COL_O0 + D * x, tmem + C::COL_S0 + 128 * x + 8 * kk,
-                       tc::smem_desc_sw128(vb + kk * 2048, C::KHALF, 1024), IPV, (acc || kk > 0));
-          tc::mma_commit(&bar[B_ODONE + x]);
+            for (int kk = 0; kk < 8; ++kk)
+              tc::mma_ts(tmem + C::COL_O0 + D * x, tmem + C::COL_S0 + 128 * x + 8 * kk,
+                         vd + ((kk * 2048) >> 4), IPV, (acc || kk > 0));
+            tc::mma_commit(&bar[B_ODONE + x]);
+          }
+          __syncwarp();
         };
         uint32_t ring = 0, qn[2] = {0, 0}, stp[2] = {0, 0};
         bool ok = true;
         for (int rnd = 0, k = snake_atom(0); ok && k < n_atoms; k = snake_atom(++rnd)) {
           Atom at;
           if (!load_atom(k, at)) continue;
-          ok = mbar_wait_bounded(&bar[B_QREADY + 0], qn[0] & 1) &&
-               mbar_wait_bounded(&bar[B_KFULL + (ring & 1)], (ring >> 1) & 1);
+          ok = wait(B_QREADY + 0, qn[0] & 1) && wait(B_KFULL + (ring & 1), (ring >> 1) & 1);
           ++qn[0];
           if (!ok) break;
           tc::fence_after();
           qk(0, ring);
           if (at.has_b) {
-            ok = mbar_wait_bounded(&bar[B_QREADY + 1], qn[1] & 1);
+            ok = wait(B_QREADY + 1, qn[1] & 1);
             ++qn[1];
             if (!ok) break;
             tc::fence_after();
             qk(1, ring);
           }
+          commit(B_KEMPTY + (ring & 1));
           for (int t = 0; t < at.n_kv; ++t) {
             const uint32_t r = ring + t;
-            ok = mbar_wait_bounded(&bar[B_VFULL + (r & 1)], (r >> 1) & 1) &&
-                 mbar_wait_bounded(&bar[B_PFULL + 0], stp[0] & 1);
+            ok = wait(B_VFULL + (r & 1), (r >> 1) & 1) && wait(B_PFULL + 0, stp[0] & 1);
             if (!ok) break;
             tc::fence_after();
             pv(0, r, t > 0);
             ++stp[0];
             if (t + 1 < at.n_kv) {
-              ok = mbar_wait_bounded(&bar[B_KFULL + ((r + 1) & 1)], ((r + 1) >> 1) & 1);
+              ok = wait(B_KFULL + ((r + 1) & 1), ((r + 1) >> 1) & 1);
               if (!ok) break;
               tc::fence_after();
               qk(0, r + 1);
             }
             if (at.has_b) {
-              ok = mbar_wait_bounded(&bar[B_PFULL + 1], stp[1] & 1);
+              ok = wait(B_PFULL + 1, stp[1] & 1);
               if (!ok) break;
               tc::fence_after();
               pv(1, r, t > 0);
               ++stp[1];
             }
-            tc::mma_commit(&bar[B_KVEMPTY + (r & 1)]);
-            if (at.has_b && t + 1 < at.n_kv) qk(1, r + 1);
+            commit(B_VEMPTY + (r & 1));
+            if (t + 1 < at.n_kv) {
+              if (at.has_b) qk(1, r + 1);
+              commit(B_KEMPTY + ((r + 1) & 1));
+            }
           }
           ring += at.n_kv;
         }
-        if (!ok) set_dev_error(a.header, DS_DEVERR_WORKLIST);
+        if (!ok && lane == 0) set_dev_error(a.header, DS_DEVERR_WORKLIST);
       }
       __syncwarp();
       // free tensor memory once every softmax thread has read its last values
