@@ -46,11 +46,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # while the hash of the kernel's source files still matches the capture.
 NCU_TRAFFIC = {
     # decode_split_kernel on the first 64 sequences of the decode-only batch:
-    # 2.290050 GB read + 6.12 MB written for 2.2576 GB algorithmic (x1.0171);
+    # 2.290066 GB read + 5.18 MB written for 2.2576 GB algorithmic (x1.0167);
     # scaled to the full batch by its algorithmic bytes (the KV read dominates
     # and grows in proportion).
-    "decode256_mha_d128": {"bytes": 9.378e9, "files": ["decode.cu", "common.cuh", "tc.cuh"],
-                           "src": "d957cf9b6883d1cc"},
+    "decode256_mha_d128": {"bytes": 9.374e9, "files": ["decode.cu", "common.cuh", "tc.cuh"],
+                           "src": "375942234a7586c8"},
+    # prefill_tc_kernel on the whole chunked-prefill workload (< 1 GB on the
+    # device, captured at full size): 706.78 MB read + 225.55 MB written.
+    "chunked_prefill_2x8192": {"bytes": 9.32339e8, "files": ["prefill_tc.cu", "common.cuh", "tc.cuh"],
+                               "src": "f26cb22ffcdc8c31"},
 }
 
 
