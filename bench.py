@@ -283,12 +283,24 @@ def gpu_arm(args, wl):
         meta_build_us = 1e6 * (time.perf_counter() - t0)
         out = torch.empty((wl.n_tokens, wl.n_q_heads * wl.head_dim), dtype=qkv.dtype, device=dev)
     m = layer.meta
-    launches_per_step = 1 + (m.n_prefill_tiles > 0) + (m.n_decode_items > 0) + \
-        (m.n_decode_items > m.n_decode_seqs)
+    fused = args.path == "fused"
+    if fused:
+        # append of prefill tokens, prefill tiles, decode rows (append + split-K,
+        # with the merge inside while the grid is at most two waves)
+        sms = torch.cuda.get_device_properties(local).multi_processor_count
+        merge_inside = m.n_decode_items * wl.n_kv_heads <= 6 * sms
+        launches_per_step = (m.n_prefill_seqs > 0) + (m.n_prefill_tiles > 0) + (m.n_decode_items > 0) + \
+            (not merge_inside and m.n_decode_items > m.n_decode_seqs)
+    else:
+        launches_per_step = 1 + (m.n_prefill_tiles > 0) + (m.n_decode_items > 0) + \
+            (m.n_decode_items > m.n_decode_seqs)
 
     def step():
-        layer.append(qkv, pool)
-        layer.attention(qkv, pool, out)
+        if fused:
+            layer.fused(qkv, pool, out)
+        else:
+            layer.append(qkv, pool)
+            layer.attention(qkv, pool, out)
 
     flush = None
     step_bytes = alg["bytes"]
@@ -313,9 +325,13 @@ def gpu_arm(args, wl):
             for k in range(K):
                 a, b, c = ev[k]
                 a.record(stream)
-                layer.append(qkv, pool)
-                b.record(stream)
-                layer.attention(qkv, pool, out)
+                if fused:
+                    b.record(stream)
+                    layer.fused(qkv, pool, out)
+                else:
+                    layer.append(qkv, pool)
+                    b.record(stream)
+                    layer.attention(qkv, pool, out)
                 c.record(stream)
                 if flush is not None:
                     flush.zero_()
@@ -329,26 +345,30 @@ def gpu_arm(args, wl):
     ms_per_step = total_ms / K
     value = ws * wl.n_tokens * K / (total_ms / 1e3)
 
-    # roofline of the attention call (the dominant launches)
+    # roofline of the attention call (the dominant launches); the fused call
+    # also does the append, so it is held to the whole step's work
     attn_mean_s = float(np.mean(attn_ms)) / 1e3
-    hbm_t = alg["attn_bytes"] / (peaks["hbm_gbs"] * 1e9)
-    tc_t = alg["attn_flops"] / (peaks["bf16_tflops"] * 1e12)
+    r_bytes = alg["bytes"] if fused else alg["attn_bytes"]
+    r_flops = alg["flops"] if fused else alg["attn_flops"]
+    hbm_t = r_bytes / (peaks["hbm_gbs"] * 1e9)
+    tc_t = r_flops / (peaks["bf16_tflops"] * 1e12)
     if hbm_t >= tc_t:
-        achieved = alg["attn_bytes"] / attn_mean_s / 1e9
+        achieved = r_bytes / attn_mean_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"]}
     else:
-        achieved = alg["attn_flops"] / attn_mean_s / 1e12
+        achieved = r_flops / attn_mean_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"]}
-    rec = NCU_TRAFFIC.get(wl.name)
+    rec = NCU_TRAFFIC.get(wl.name + (":fused" if fused else ""))
     roof["traffic"] = rec["bytes"] if rec and rec.get("src") == _src_hash(rec["files"]) else None
-    roof["kernel"] = "ds_blocked_attention launches (%s)" % (
-        "decode split-K + combine" if m.n_prefill_tiles == 0 else
-        "prefill tiles" if m.n_decode_items == 0 else "prefill tiles + decode split-K + combine")
+    parts = ("decode split-K + combine" if m.n_prefill_tiles == 0 else
+             "prefill tiles" if m.n_decode_items == 0 else "prefill tiles + decode split-K + combine")
+    roof["kernel"] = ("ds_fused_append_attention launches (%s, append inside)" % parts if fused
+                      else "ds_blocked_attention launches (%s)" % parts)
     roof["peak_source"] = peaks["source"]
-    roof["algorithmic_bytes"] = alg["attn_bytes"]
-    roof["algorithmic_flops"] = alg["attn_flops"]
+    roof["algorithmic_bytes"] = r_bytes
+    roof["algorithmic_flops"] = r_flops
     roof["mean_ms"] = attn_mean_s * 1e3
 
     # whole-step roofline (slower of bytes/BW and flops/peak) as a fraction
@@ -393,7 +413,7 @@ def gpu_arm(args, wl):
                        "kv_history_tokens": int(wl.seen.sum()), "n_q_heads": wl.n_q_heads,
                        "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim, "block_size": 64,
                        "rope_theta": wl.rope_theta, "seed": wl.seed, "l2": l2_note,
-                       "parallelism": "replicas" if ws > 1 else "single"},
+                       "path": args.path, "parallelism": "replicas" if ws > 1 else "single"},
             "roofline": roof,
             "step_roofline_frac": step_frac,
             "decode_kv_gbps": alg["kv_history_bytes"] / (float(np.mean(attn_ms)) / 1e3) / 1e9,
@@ -548,8 +568,11 @@ def component_graph(args, wl):
 
     def eager():
         layer.build(descs, wl.num_blocks)
-        layer.append(qkv, pool)
-        layer.attention(qkv, pool, out)
+        if args.path == "fused":
+            layer.fused(qkv, pool, out)
+        else:
+            layer.append(qkv, pool)
+            layer.attention(qkv, pool, out)
 
     with torch.cuda.stream(st):
         for _ in range(args.warmup):
@@ -573,7 +596,7 @@ def component_graph(args, wl):
             st.synchronize()
             res[name] = (a.elapsed_time(b) / args.steps, 1e3 * (time.perf_counter() - t0) / args.steps)
     _line("ragged attn layer step, CUDA graph replay (new tokens/s)", wl.n_tokens / (res["graph"][1] / 1e3),
-          "tokens/s", {"workload": wl.name, "component": "graph"},
+          "tokens/s", {"workload": wl.name, "component": "graph", "path": args.path},
           eager_device_ms=res["eager"][0], eager_wall_ms=res["eager"][1],
           graph_device_ms=res["graph"][0], graph_wall_ms=res["graph"][1], steps=args.steps)
 
@@ -590,6 +613,9 @@ def main(argv=None):
     ap.add_argument("--part", choices=["decode", "prefill"], default=None,
                     help="profile one kernel family: keep only the decode rows or the prefill chunks")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", choices=["split", "fused"], default="split",
+                    help="split: ds_kv_rotary_append then ds_blocked_attention; "
+                         "fused: ds_fused_append_attention")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -239,6 +239,46 @@ ds_status ds_blocked_attention(const ds_ragged_meta* meta, const ds_attn_params*
                                const ds_kv_pool* pool, void* out, void* workspace,
                                size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------- fused append+attention -- */
+
+/* The append and the attention of one batch in as few launches as the batch
+ * allows.  This is operator fusion as "Principle: Deepspeedai DeepSpeed Inference Engine
+ * Init" (leeroopedia), section "Theoretical Basis", describes it: fewer, larger
+ * kernels cut launch overhead and the round trip of intermediates.  The
+ * RoPE-and-append of a decode row happens inside the attention kernel that
+ * reads the row's KV.
+ *
+ * Results: exactly those of ds_kv_rotary_append(meta, params, rope, qkv, NULL,
+ * pool) followed by ds_blocked_attention on the same stream: the same pool
+ * contents and the same output bits.
+ * Launches:
+ *  - decode rows: the split-K kernel appends each row's new K/V in the split
+ *    that holds its last block.  While its grid is at most two waves
+ *    (n_decode_items * n_kv_heads <= 6 * SMs) the last split of each (row, KV
+ *    head) also merges the partials, so a decode-only batch is 1 launch.
+ *    Larger grids merge in a separate kernel (2 launches), which costs less
+ *    there.
+ *  - prefill tiles: the append kernel over prefill tokens only, then the
+ *    prefill kernel; decode rows follow as above.
+ *
+ * Workspace: DEVICE, 256-byte aligned, ws_bytes >= ds_fused_workspace_size for
+ * the meta object's capacities.  It starts with one int32 counter per
+ * (sequence slot, KV head), which must be zero when a call starts; every call
+ * that completes without a device error leaves them zero.  Zero them once with
+ * ds_fused_workspace_init before the first call, and again after any call that
+ * set a bit in the device error word (a CTA that stops early never counts
+ * itself done).  The rest holds split partials, as for ds_blocked_attention.
+ * Errors: those of ds_kv_rotary_append and ds_blocked_attention. */
+ds_status ds_fused_workspace_size(const ds_attn_params* params, int32_t max_seqs, int32_t max_tokens,
+                                  int32_t max_blocks, size_t* bytes);
+/* Enqueue the zeroing of the workspace's counters (meta gives the capacity). */
+ds_status ds_fused_workspace_init(const ds_ragged_meta* meta, const ds_attn_params* params,
+                                  void* workspace, size_t ws_bytes, void* stream);
+ds_status ds_fused_append_attention(const ds_ragged_meta* meta, const ds_attn_params* params,
+                                    const ds_rope_table* rope, const void* qkv,
+                                    const ds_kv_pool* pool, void* out, void* workspace,
+                                    size_t ws_bytes, void* stream);
+
 /* Allocation-free variant of ds_blocked_attention.  (The source pages have no
  * counterpart: this entry point exists for callers that cannot allocate.)
  *

@@ -43,9 +43,11 @@ __global__ void __launch_bounds__(128) append_kernel(
     const int32_t* __restrict__ tok_seq, const int32_t* __restrict__ tok_pos,
     const int32_t* __restrict__ blk_off, const int32_t* __restrict__ block_table,
     const uint16_t* __restrict__ qkv, uint16_t* __restrict__ q_out, uint16_t* __restrict__ pool,
-    LayerArgs a) {
+    const int32_t* __restrict__ skip_if_single, LayerArgs a) {
   const int t = blockIdx.x;
   const int seq = tok_seq[t];
+  // decode rows are appended by the fused decode kernel
+  if (skip_if_single && skip_if_single[seq] == 1) return;
   const int p = tok_pos[t];
   const int W = (a.Hq + 2 * a.Hkv) * D;
   const uint16_t* row = qkv + (int64_t)t * W;
@@ -95,27 +97,29 @@ __global__ void __launch_bounds__(128) append_kernel(
 
 template <bool BF16, bool HALF>
 static cudaError_t launch_append_t(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                                   void* q_out, void* pool, cudaStream_t st) {
+                                   void* q_out, void* pool, cudaStream_t st, bool prefill_only) {
   dim3 grid(m.n_tokens);
+  const int32_t* skip = prefill_only ? m.seq_new : nullptr;
   if (a.D == 128)
     append_kernel<BF16, HALF, 128><<<grid, 128, 0, st>>>(
         m.tok_seq, m.tok_pos, m.blk_off, m.block_table, static_cast<const uint16_t*>(qkv),
-        static_cast<uint16_t*>(q_out), static_cast<uint16_t*>(pool), a);
+        static_cast<uint16_t*>(q_out), static_cast<uint16_t*>(pool), skip, a);
   else
     append_kernel<BF16, HALF, 64><<<grid, 128, 0, st>>>(
         m.tok_seq, m.tok_pos, m.blk_off, m.block_table, static_cast<const uint16_t*>(qkv),
-        static_cast<uint16_t*>(q_out), static_cast<uint16_t*>(pool), a);
+        static_cast<uint16_t*>(q_out), static_cast<uint16_t*>(pool), skip, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_append(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv, void* q_out,
-                          void* pool, cudaStream_t st) {
+                          void* pool, cudaStream_t st, bool prefill_only) {
   const bool half = a.style == DS_ROPE_HALF;
+  const bool po = prefill_only;
   if (a.dtype == DS_BF16)
-    return half ? launch_append_t<true, true>(m, a, qkv, q_out, pool, st)
-                : launch_append_t<true, false>(m, a, qkv, q_out, pool, st);
-  return half ? launch_append_t<false, true>(m, a, qkv, q_out, pool, st)
-              : launch_append_t<false, false>(m, a, qkv, q_out, pool, st);
+    return half ? launch_append_t<true, true>(m, a, qkv, q_out, pool, st, po)
+                : launch_append_t<true, false>(m, a, qkv, q_out, pool, st, po);
+  return half ? launch_append_t<false, true>(m, a, qkv, q_out, pool, st, po)
+              : launch_append_t<false, false>(m, a, qkv, q_out, pool, st, po);
 }
 
 }  // namespace dsr

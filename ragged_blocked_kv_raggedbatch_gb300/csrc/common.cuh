@@ -35,6 +35,7 @@ struct LayerArgs {
   int32_t max_positions;   // rotary table rows
   const float2* rope;      // [max_positions][D/2]
   int32_t* header;         // device error word lives at header[HDR_ERR]
+  int32_t split_blocks;    // KV blocks per decode split
 };
 
 // ----------------------------------------------------------- device helpers --
@@ -198,13 +199,21 @@ void set_last_error(const char* msg);
 // Implemented in the .cu files; called by the host layer after validation.
 cudaError_t launch_rope_table(const ds_attn_params& p, int32_t max_positions, float2* table,
                               cudaStream_t st);
+// prefill_only: tokens of decode rows (sequences with one new token) are left
+// to the fused decode kernel.
 cudaError_t launch_append(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                          void* q_out, void* pool, cudaStream_t st);
+                          void* q_out, void* pool, cudaStream_t st, bool prefill_only = false);
 // overlap_previous: launch as a programmatic dependent of the kernel before it
 // on the stream (the prefill kernel), so decode CTAs can start while it runs.
+// fused_append: the kernel also appends each decode row's new K/V (the append
+// kernel then skips decode rows).  counters == nullptr: split partials are
+// merged by a separate combine launch; counters != nullptr (fused_append only;
+// zero on entry, zero again on exit): the last split CTA of every (row, KV
+// head) merges them.
 cudaError_t launch_decode(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
                           const void* pool, void* out, float* ws, cudaStream_t st,
-                          bool overlap_previous);
+                          bool overlap_previous, bool fused_append = false,
+                          int32_t* counters = nullptr);
 cudaError_t launch_prefill(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
                            const void* pool, void* out, cudaStream_t st);
 

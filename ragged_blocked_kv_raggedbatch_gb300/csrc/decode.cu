@@ -17,6 +17,15 @@
 // merged at the end of the split.  A split emits (m, l, o[D]) per query head
 // in fp32 (m in log2 units), or the final row when it is its sequence's only
 // split; the combine kernel merges the splits of the others.
+//
+// Fused variant (FUSED): the split holding a row's last KV block also appends
+// the row's new token: it rotates K (the append kernel's arithmetic, so the
+// stored bits are the same), writes K and V into the pool slot and patches
+// them into its staged copy of that block, whose slot the bulk copy read before
+// the write.  With a counter array, the splits of a multi-split row also count
+// themselves done on a per-(sequence, KV head) counter after writing their
+// partials; the last one merges all partials (the combine kernel's arithmetic,
+// in its order) and resets the counter, so the decode rows need one launch.
 #include "tc.cuh"
 
 // CTA shape: warps per CTA, bulk-copy pipeline stages (each stage one K + V
@@ -76,13 +85,13 @@ struct DecodeCfg {
   static_assert(MERGE_FLOATS * 4 <= TILES_BYTES, "merge scratch aliases the tiles");
 };
 
-template <bool BF16, bool HALF, int D, int G, int WARPS, int STAGES>
+template <bool BF16, bool HALF, int D, int G, int WARPS, int STAGES, bool FUSED>
 __global__ void __launch_bounds__(WARPS * 32, G >= 4 ? DSR_DECODE_MINB_GQA : DSR_DECODE_MINB) decode_split_kernel(
     const int4* __restrict__ items, const int32_t* __restrict__ cu_seqlens,
     const int32_t* __restrict__ seq_seen, const int32_t* __restrict__ blk_off,
     const int32_t* __restrict__ block_table, const uint16_t* __restrict__ qkv,
-    const uint16_t* __restrict__ pool, uint16_t* __restrict__ out, float* __restrict__ ws,
-    int32_t n_items, LayerArgs a) {
+    uint16_t* __restrict__ pool, uint16_t* __restrict__ out, float* __restrict__ ws,
+    int32_t* __restrict__ counters, int32_t n_items, LayerArgs a) {
   using C = DecodeCfg<BF16, HALF, D, G, WARPS, STAGES>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -125,6 +134,41 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 4 ? DSR_DECODE_MINB_GQA : DSR
   };
   if (tid == 0) {
     for (int s = 0; s < STAGES && s < nblk; ++s) issue(s, b_begin + s);
+  }
+
+  // ---- fused append of the row's new token (position p) by the split that
+  // holds its block: lanes [0, D/16) rotate one 16-element unit of K each,
+  // lanes [0, D/8) copy 8 elements of V each.
+  const int nb = (L + kBlockSize - 1) / kBlockSize;
+  const bool owner = FUSED && b_end == nb;
+  const int new_off = p % kBlockSize;
+  const int ki0 = HALF ? 8 * lane : 16 * lane;
+  const int ki1 = HALF ? D / 2 + 8 * lane : 16 * lane + 8;
+  uint4 kn0 = make_uint4(0, 0, 0, 0), kn1 = kn0, vn = kn0;
+  if (owner && warp == 0) {
+    const int blk = btab[p / kBlockSize];
+    const bool blk_ok = blk >= 0 && blk < a.num_blocks;  // else reported by issue()
+    const uint16_t* row = qkv + (int64_t)t * (a.Hq + 2 * a.Hkv) * D;
+    if (lane < D / 16) {
+      kn0 = ld_nc_v4(row + (a.Hq + c) * D + ki0);
+      kn1 = ld_nc_v4(row + (a.Hq + c) * D + ki1);
+      float4 cs[4];
+      const float4* cs_row = reinterpret_cast<const float4*>(a.rope + (int64_t)p * (D / 2));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) cs[q] = __ldg(cs_row + 4 * lane + q);  // pairs 8*lane ..
+      rotate16<BF16, HALF>(kn0, kn1, cs);
+      if (blk_ok) {
+        uint16_t* dst = pool + ((((int64_t)blk * 2 + 0) * a.Hkv + c) * kBlockSize + new_off) * D;
+        *reinterpret_cast<uint4*>(dst + ki0) = kn0;
+        *reinterpret_cast<uint4*>(dst + ki1) = kn1;
+      }
+    }
+    if (lane < D / 8) {
+      vn = ld_nc_v4(row + (a.Hq + a.Hkv + c) * D + 8 * lane);
+      if (blk_ok)
+        *reinterpret_cast<uint4*>(pool + ((((int64_t)blk * 2 + 1) * a.Hkv + c) * kBlockSize + new_off) * D +
+                                  8 * lane) = vn;
+    }
   }
 
   // ---- query: rotate (fp32, same rule as the append), scale into log2 units.
@@ -186,6 +230,19 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 4 ? DSR_DECODE_MINB_GQA : DSR
     const uint16_t* Kt = reinterpret_cast<const uint16_t*>(smem + stage * C::STAGE_BYTES);
     const uint16_t* Vt = Kt + kBlockSize * D;
     const int kbase = (b_begin + j) * kBlockSize;
+    if (owner && j == nblk - 1) {
+      // the new token's slot in the staged last block: the values just appended
+      if (warp == 0) {
+        uint16_t* Kw = reinterpret_cast<uint16_t*>(smem + stage * C::STAGE_BYTES) + new_off * D;
+        uint16_t* Vw = Kw + kBlockSize * D;
+        if (lane < D / 16) {
+          *reinterpret_cast<uint4*>(Kw + ki0) = kn0;
+          *reinterpret_cast<uint4*>(Kw + ki1) = kn1;
+        }
+        if (lane < D / 8) *reinterpret_cast<uint4*>(Vw + 8 * lane) = vn;
+      }
+      __syncthreads();
+    }
 
     // scores of this group's KPG keys, partial over the lane's 8 dims
     float part[G][C::KPG];
@@ -330,6 +387,49 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 4 ? DSR_DECODE_MINB_GQA : DSR
       *reinterpret_cast<float4*>(wo + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
   }
+
+  if (FUSED && counters != nullptr && slot >= 0) {
+    // ---- the last split of (row, KV head c) to finish merges all partials
+    __shared__ int s_last;
+    const int split = a.split_blocks;
+    const int cnt = (nb + split - 1) / split;
+    const int first = slot - b_begin / split;  // a row's splits hold consecutive slots
+    // every thread's partials precede thread 0's fence (barrier), which
+    // precedes the count: whoever counts last sees them all
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      s_last = atomicAdd(&counters[seq * a.Hkv + c], 1) == cnt - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const float* wo_base = ws + (int64_t)n_items * a.Hq * 2;
+    for (int u = tid; u < units; u += WARPS * 32) {
+      const int h = u / (D / 8), d8 = u % (D / 8);
+      const int hq = c * G + h;
+      float M = kNegBig;
+      for (int k = 0; k < cnt; ++k) M = fmaxf(M, __ldcg(ws + ((int64_t)(first + k) * a.Hq + hq) * 2));
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, lsum = 0.f;
+      for (int k = 0; k < cnt; ++k) {
+        const float* ml = ws + ((int64_t)(first + k) * a.Hq + hq) * 2;
+        const float sc = fast_exp2(__ldcg(ml) - M);
+        lsum += sc * __ldcg(ml + 1);
+        const float4* src =
+            reinterpret_cast<const float4*>(wo_base + ((int64_t)(first + k) * a.Hq + hq) * D + 8 * d8);
+        const float4 s0 = __ldcg(src), s1 = __ldcg(src + 1);
+        acc[0] += sc * s0.x; acc[1] += sc * s0.y; acc[2] += sc * s0.z; acc[3] += sc * s0.w;
+        acc[4] += sc * s1.x; acc[5] += sc * s1.y; acc[6] += sc * s1.z; acc[7] += sc * s1.w;
+      }
+      const float inv = 1.f / lsum;
+      uint4 pk;
+      uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pw[e] = Stor<BF16>::pack(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+      *reinterpret_cast<uint4*>(out + (int64_t)t * a.Hq * D + hq * D + 8 * d8) = pk;
+    }
+    if (tid == 0) counters[seq * a.Hkv + c] = 0;  // ready for the next launch
+  }
 }
 
 // Merge the splits of each multi-split decode row: one warp per (row, head).
@@ -375,11 +475,12 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const int4* __restr
 template <bool BF16, bool HALF, int D, int G>
 static cudaError_t launch_decode_t(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
                                    const void* pool, void* out, float* ws, cudaStream_t st,
-                                   bool overlap_previous) {
+                                   bool overlap_previous, bool fused, int32_t* counters) {
   constexpr int WARPS = G >= 4 ? DSR_DECODE_WARPS_GQA : DSR_DECODE_WARPS;
   constexpr int STAGES = G >= 4 ? DSR_DECODE_STAGES_GQA : DSR_DECODE_STAGES;
   using C = DecodeCfg<BF16, HALF, D, G, WARPS, STAGES>;
-  auto kern = decode_split_kernel<BF16, HALF, D, G, WARPS, STAGES>;
+  auto kern = fused ? decode_split_kernel<BF16, HALF, D, G, WARPS, STAGES, true>
+                    : decode_split_kernel<BF16, HALF, D, G, WARPS, STAGES, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -396,14 +497,15 @@ static cudaError_t launch_decode_t(const ds_ragged_meta& m, const LayerArgs& a, 
   // write disjoint output rows.
   cfg.attrs = attr;
   cfg.numAttrs = overlap_previous ? 1 : 0;
+  // the unfused kernel only reads the pool (the append kernel wrote the rows)
   e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const int4*>(m.decode_items), m.cu_seqlens,
                          m.seq_seen, m.blk_off, m.block_table, static_cast<const uint16_t*>(qkv),
-                         static_cast<const uint16_t*>(pool), static_cast<uint16_t*>(out), ws,
-                         (int32_t)m.n_decode_items, a);
+                         static_cast<uint16_t*>(const_cast<void*>(pool)), static_cast<uint16_t*>(out), ws,
+                         counters, (int32_t)m.n_decode_items, a);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (m.n_decode_items > m.n_decode_seqs) {
+  if (counters == nullptr && m.n_decode_items > m.n_decode_seqs) {
     dim3 g2(m.n_decode_seqs, (a.Hq + 3) / 4);
     decode_combine_kernel<BF16, D><<<g2, 128, 0, st>>>(
         reinterpret_cast<const int4*>(m.decode_seqs), ws, static_cast<uint16_t*>(out),
@@ -415,33 +517,35 @@ static cudaError_t launch_decode_t(const ds_ragged_meta& m, const LayerArgs& a, 
 
 template <bool BF16, bool HALF, int D>
 static cudaError_t launch_decode_g(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                                   const void* pool, void* out, float* ws, cudaStream_t st, bool ov) {
+                                   const void* pool, void* out, float* ws, cudaStream_t st, bool ov,
+                                   bool fu, int32_t* cnt) {
   switch (a.G) {
-    case 1: return launch_decode_t<BF16, HALF, D, 1>(m, a, qkv, pool, out, ws, st, ov);
-    case 2: return launch_decode_t<BF16, HALF, D, 2>(m, a, qkv, pool, out, ws, st, ov);
-    case 4: return launch_decode_t<BF16, HALF, D, 4>(m, a, qkv, pool, out, ws, st, ov);
-    case 8: return launch_decode_t<BF16, HALF, D, 8>(m, a, qkv, pool, out, ws, st, ov);
+    case 1: return launch_decode_t<BF16, HALF, D, 1>(m, a, qkv, pool, out, ws, st, ov, fu, cnt);
+    case 2: return launch_decode_t<BF16, HALF, D, 2>(m, a, qkv, pool, out, ws, st, ov, fu, cnt);
+    case 4: return launch_decode_t<BF16, HALF, D, 4>(m, a, qkv, pool, out, ws, st, ov, fu, cnt);
+    case 8: return launch_decode_t<BF16, HALF, D, 8>(m, a, qkv, pool, out, ws, st, ov, fu, cnt);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <bool BF16, bool HALF>
 static cudaError_t launch_decode_d(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                                   const void* pool, void* out, float* ws, cudaStream_t st, bool ov) {
-  return a.D == 128 ? launch_decode_g<BF16, HALF, 128>(m, a, qkv, pool, out, ws, st, ov)
-                    : launch_decode_g<BF16, HALF, 64>(m, a, qkv, pool, out, ws, st, ov);
+                                   const void* pool, void* out, float* ws, cudaStream_t st, bool ov,
+                                   bool fu, int32_t* cnt) {
+  return a.D == 128 ? launch_decode_g<BF16, HALF, 128>(m, a, qkv, pool, out, ws, st, ov, fu, cnt)
+                    : launch_decode_g<BF16, HALF, 64>(m, a, qkv, pool, out, ws, st, ov, fu, cnt);
 }
 
 cudaError_t launch_decode(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
                           const void* pool, void* out, float* ws, cudaStream_t st,
-                          bool overlap_previous) {
+                          bool overlap_previous, bool fused_append, int32_t* counters) {
   const bool half = a.style == DS_ROPE_HALF;
-  const bool ov = overlap_previous;
+  const bool ov = overlap_previous, fu = fused_append;
   if (a.dtype == DS_BF16)
-    return half ? launch_decode_d<true, true>(m, a, qkv, pool, out, ws, st, ov)
-                : launch_decode_d<true, false>(m, a, qkv, pool, out, ws, st, ov);
-  return half ? launch_decode_d<false, true>(m, a, qkv, pool, out, ws, st, ov)
-              : launch_decode_d<false, false>(m, a, qkv, pool, out, ws, st, ov);
+    return half ? launch_decode_d<true, true>(m, a, qkv, pool, out, ws, st, ov, fu, counters)
+                : launch_decode_d<true, false>(m, a, qkv, pool, out, ws, st, ov, fu, counters);
+  return half ? launch_decode_d<false, true>(m, a, qkv, pool, out, ws, st, ov, fu, counters)
+              : launch_decode_d<false, false>(m, a, qkv, pool, out, ws, st, ov, fu, counters);
 }
 
 }  // namespace dsr

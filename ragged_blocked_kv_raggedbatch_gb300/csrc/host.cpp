@@ -117,6 +117,7 @@ dsr::LayerArgs layer_args(const ds_ragged_meta* m, const ds_attn_params* p,
   a.max_positions = r->max_positions;
   a.rope = static_cast<const float2*>(r->table);
   a.header = m->header;
+  a.split_blocks = m->split_blocks;
   return a;
 }
 
@@ -462,6 +463,88 @@ ds_status ds_blocked_attention(const ds_ragged_meta* meta, const ds_attn_params*
     cudaError_t e = dsr::launch_decode(*meta, a, qkv, pool->base, out, static_cast<float*>(workspace), st,
                                        meta->n_prefill_tiles > 0);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernels");
+  }
+  return DS_OK;
+}
+
+static int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 1;
+  return n;
+}
+
+// Fused workspace: [counters: max_seqs * n_kv_heads int32, 256-aligned][split partials].
+static size_t fused_counter_bytes(const ds_attn_params* params, int32_t max_seqs) {
+  return align_up((size_t)std::max(max_seqs, 0) * (size_t)params->n_kv_heads * sizeof(int32_t), 256);
+}
+
+ds_status ds_fused_workspace_size(const ds_attn_params* params, int32_t max_seqs, int32_t max_tokens,
+                                  int32_t max_blocks, size_t* bytes) {
+  size_t part = 0;
+  if (ds_status s = ds_blocked_attention_workspace_size(params, max_seqs, max_tokens, max_blocks, &part))
+    return s;
+  *bytes = fused_counter_bytes(params, max_seqs) + part;
+  return DS_OK;
+}
+
+ds_status ds_fused_workspace_init(const ds_ragged_meta* meta, const ds_attn_params* params,
+                                  void* workspace, size_t ws_bytes, void* stream) {
+  if (ds_status s = check_params(params)) return s;
+  if (!meta) return fail(DS_ERR_INVALID_ARG, "meta is NULL");
+  if (!workspace || !aligned(workspace, 256))
+    return fail(DS_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
+  const size_t cb = fused_counter_bytes(params, meta->max_seqs);
+  if (ws_bytes < cb) return fail(DS_ERR_WORKSPACE, "workspace holds %zu bytes, the counters need %zu", ws_bytes, cb);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, cb, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "zeroing the workspace counters");
+  return DS_OK;
+}
+
+ds_status ds_fused_append_attention(const ds_ragged_meta* meta, const ds_attn_params* params,
+                                    const ds_rope_table* rope, const void* qkv,
+                                    const ds_kv_pool* pool, void* out, void* workspace,
+                                    size_t ws_bytes, void* stream) {
+  if (ds_status s = check_params(params)) return s;
+  if (ds_status s = check_meta(meta)) return s;
+  if (meta->n_tokens == 0) return DS_OK;
+  if (ds_status s = check_rope(rope, params, meta)) return s;
+  if (ds_status s = check_pool(pool, meta)) return s;
+  if (!qkv || !aligned(qkv, 16)) return fail(DS_ERR_INVALID_ARG, "qkv NULL or not 16-byte aligned");
+  if (!out || !aligned(out, 16)) return fail(DS_ERR_INVALID_ARG, "out NULL or not 16-byte aligned");
+  const size_t cb = fused_counter_bytes(params, meta->max_seqs);
+  const size_t need = cb + (size_t)meta->n_decode_items * (size_t)params->n_q_heads *
+                               (size_t)(params->head_dim + 2) * sizeof(float);
+  if (meta->n_decode_items > 0) {
+    if (!workspace || !aligned(workspace, 256))
+      return fail(DS_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
+    if (ws_bytes < need)
+      return fail(DS_ERR_WORKSPACE, "workspace holds %zu bytes, this batch needs %zu", ws_bytes, need);
+  }
+  dsr::LayerArgs a = layer_args(meta, params, rope, pool->num_blocks);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (meta->n_prefill_seqs > 0) {
+    cudaError_t e = dsr::launch_append(*meta, a, qkv, nullptr, pool->base, st, /*prefill_only=*/true);
+    if (e != cudaSuccess) return cuda_fail(e, "append kernel");
+  }
+  if (meta->n_prefill_tiles > 0) {
+    cudaError_t e = dsr::launch_prefill(*meta, a, qkv, pool->base, out, st);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill kernel");
+  }
+  if (meta->n_decode_items > 0) {
+    // Merge split partials inside the decode kernel (the decode rows are then
+    // one launch) while its grid is at most two waves of 3 CTAs per SM.  On a
+    // larger grid the separate merge launch costs less than holding every CTA
+    // for its count: decode-only batch of 256 rows on GB300, 1.304 ms merged in
+    // the kernel against 1.297 ms with the merge kernel.
+    const bool merge_in_kernel =
+        (int64_t)meta->n_decode_items * params->n_kv_heads <= 6LL * device_sm_count();
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    cudaError_t e = dsr::launch_decode(*meta, a, qkv, pool->base, out, reinterpret_cast<float*>(w + cb), st,
+                                       meta->n_prefill_tiles > 0, /*fused_append=*/true,
+                                       merge_in_kernel ? reinterpret_cast<int32_t*>(w) : nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "fused decode kernel");
   }
   return DS_OK;
 }

@@ -80,6 +80,9 @@ SIGNATURES = {
     "ds_blocked_attention": (i32, [P, P, P, P, P, P, P, ctypes.c_size_t, P]),
     "ds_get_device_error": (i32, [P, P, P]),
     "ds_blocked_attention_static_ws": (i32, [P, P, P, P, P, P, P]),
+    "ds_fused_workspace_size": (i32, [P, i32, i32, i32, P]),
+    "ds_fused_workspace_init": (i32, [P, P, P, ctypes.c_size_t, P]),
+    "ds_fused_append_attention": (i32, [P, P, P, P, P, P, P, ctypes.c_size_t, P]),
     "ds_block_allocator_init": (i32, [P, P, P, i32, P]),
     "ds_block_allocator_allocate": (i32, [P, i32, P]),
     "ds_block_allocator_free": (i32, [P, P, i32]),
@@ -232,6 +235,28 @@ def ds_blocked_attention(meta: ds_ragged_meta, params: ds_attn_params, rope: ds_
            "ds_blocked_attention")
 
 
+def ds_fused_workspace_size(params: ds_attn_params, max_seqs: int, max_tokens: int, max_blocks: int) -> int:
+    b = ctypes.c_size_t(0)
+    _check(load().ds_fused_workspace_size(_ref(params), max_seqs, max_tokens, max_blocks, _ref(b)),
+           "ds_fused_workspace_size")
+    return b.value
+
+
+def ds_fused_workspace_init(meta: ds_ragged_meta, params: ds_attn_params, workspace, stream=None):
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().ds_fused_workspace_init(_ref(meta), _ref(params), _ptr(workspace), ws_bytes, _stream(stream)),
+           "ds_fused_workspace_init")
+
+
+def ds_fused_append_attention(meta: ds_ragged_meta, params: ds_attn_params, rope: ds_rope_table, qkv,
+                              pool: ds_kv_pool, out, workspace, stream=None):
+    """The append and the attention of one batch (a decode-only batch is one launch)."""
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().ds_fused_append_attention(_ref(meta), _ref(params), _ref(rope), _ptr(qkv), _ref(pool),
+                                            _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)),
+           "ds_fused_append_attention")
+
+
 def ds_blocked_attention_static_ws(meta: ds_ragged_meta, params: ds_attn_params, rope: ds_rope_table,
                                    qkv, pool: ds_kv_pool, out, stream=None):
     """ds_blocked_attention with the split partials in the library's built-in
@@ -333,6 +358,7 @@ class RaggedLayer:
         self.rope = ds_rope_table_build(params, max_positions, self.rope_buf, stream)
         wb = ds_blocked_attention_workspace_size(params, max_seqs, max_tokens, max_blocks)
         self.workspace = torch.empty(wb, dtype=torch.uint8, device=device)
+        self.fused_ws = None  # made (and its counters zeroed) on the first fused call
 
     def build(self, descs: SeqDescs, pool_num_blocks: int):
         ds_ragged_meta_build(descs, self.params, pool_num_blocks, self.meta, self.stream)
@@ -344,6 +370,17 @@ class RaggedLayer:
     def attention(self, qkv, pool_t, out):
         pool = ds_kv_pool(pool_t.data_ptr(), pool_t.shape[0])
         ds_blocked_attention(self.meta, self.params, self.rope, qkv, pool, out, self.workspace, self.stream)
+
+    def fused(self, qkv, pool_t, out):
+        """Append + attention in one call (ds_fused_append_attention)."""
+        import torch
+        if self.fused_ws is None:
+            m = self.meta
+            fb = ds_fused_workspace_size(self.params, m.max_seqs, m.max_tokens, m.max_blocks)
+            self.fused_ws = torch.empty(fb, dtype=torch.uint8, device=self.device)
+            ds_fused_workspace_init(self.meta, self.params, self.fused_ws, self.stream)
+        pool = ds_kv_pool(pool_t.data_ptr(), pool_t.shape[0])
+        ds_fused_append_attention(self.meta, self.params, self.rope, qkv, pool, out, self.fused_ws, self.stream)
 
     def device_error(self) -> int:
         return ds_get_device_error(self.meta, self.stream)

@@ -239,6 +239,39 @@ def test_call_validation_before_launch(lib):
     assert lib.ds_kv_rotary_append(None, R._ref(p), R._ref(rope), FAKE_DEV, None, R._ref(pool), None) == R.DS_ERR_INVALID_ARG
 
 
+def test_fused_call_validation_before_launch(lib):
+    """ds_fused_* reject bad arguments on the host; the fused workspace is the
+    split-path workspace plus one int32 counter per (sequence slot, KV head)."""
+    wl = W.make_custom([(70, 3), (5, 1), (200, 1)], 4, 2, 64, extra_blocks=1)
+    pk = Packed(wl)
+    assert pk.pack() == R.DS_OK
+    p = pk.params
+    rope = R.ds_rope_table(FAKE_DEV, wl.max_len(), 64, float(wl.rope_theta))
+    pool = R.ds_kv_pool(FAKE_DEV, wl.num_blocks)
+    ms, mt, mb = pk.meta.max_seqs, pk.meta.max_tokens, pk.meta.max_blocks
+    split, fused = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.ds_blocked_attention_workspace_size(R._ref(p), ms, mt, mb, R._ref(split)) == R.DS_OK
+    assert lib.ds_fused_workspace_size(R._ref(p), ms, mt, mb, R._ref(fused)) == R.DS_OK
+    counters = -(-ms * p.n_kv_heads * 4 // 256) * 256
+    assert fused.value == split.value + counters
+    call = lambda **kw: lib.ds_fused_append_attention(
+        R._ref(pk.meta), R._ref(p), R._ref(kw.get("rope", rope)), kw.get("qkv", FAKE_DEV),
+        R._ref(kw.get("pool", pool)), kw.get("out", FAKE_DEV), kw.get("ws", FAKE_DEV),
+        kw.get("ws_bytes", fused.value), None)
+    assert call(out=None) == R.DS_ERR_INVALID_ARG
+    assert call(qkv=FAKE_DEV + 2) == R.DS_ERR_INVALID_ARG
+    need = counters + pk.meta.n_decode_items * p.n_q_heads * (p.head_dim + 2) * 4
+    assert pk.meta.n_decode_items > 0
+    assert call(ws_bytes=need - 4) == R.DS_ERR_WORKSPACE
+    assert call(ws=FAKE_DEV + 64) == R.DS_ERR_INVALID_ARG
+    assert call(rope=R.ds_rope_table(FAKE_DEV, wl.max_len() - 1, 64, float(wl.rope_theta))) == R.DS_ERR_CAPACITY
+    assert call(pool=R.ds_kv_pool(FAKE_DEV, wl.num_blocks + 1)) == R.DS_ERR_INVALID_ARG
+    init = lambda ws, nbytes: lib.ds_fused_workspace_init(R._ref(pk.meta), R._ref(p), ws, nbytes, None)
+    assert init(FAKE_DEV, 16) == R.DS_ERR_WORKSPACE
+    assert init(FAKE_DEV + 64, fused.value) == R.DS_ERR_INVALID_ARG
+    assert init(None, fused.value) == R.DS_ERR_INVALID_ARG
+
+
 def test_offload_restore_and_gather_validation(lib):
     """Argument errors of the data-movement calls are found on the host."""
     p = R.make_params(8, 2, 128)

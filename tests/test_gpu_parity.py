@@ -92,6 +92,8 @@ def test_empty_batch_is_a_no_op():
 # ------------------------------------------------------------------ full size
 
 FULL = ["decode256_mha_d128", "splitfuse2048_gqa_d128", "chunked_prefill_2x8192", "max_ragged_8192"]
+# the workloads whose lengths are drawn at random, also checked at seeds 1 and 2
+RANDOM_LENGTHS = ["decode256_mha_d128", "splitfuse2048_gqa_d128", "max_ragged_8192"]
 
 
 def _pick_sequences(wl, rng, n_pre=4, n_dec=12):
@@ -105,10 +107,10 @@ def _pick_sequences(wl, rng, n_pre=4, n_dec=12):
     return sorted(set(int(i) for i in pick))
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled(name):
-    wl = W.make_workload(name, 0)
-    rng = np.random.default_rng(1234)
+@pytest.mark.parametrize("name,seed", [(n, 0) for n in FULL] + [(n, s) for n in RANDOM_LENGTHS for s in (1, 2)])
+def test_full_size_sampled(name, seed):
+    wl = W.make_workload(name, seed)
+    rng = np.random.default_rng(1234 + seed)
     qkv, pool = W.make_values(wl, "cuda")
     seqs = _pick_sequences(wl, rng)
     sub, pool_c, qkv_c, gidx, old_ids = compact(wl, seqs, pool, qkv)
