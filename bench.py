@@ -46,15 +46,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # while the hash of the kernel's source files still matches the capture.
 NCU_TRAFFIC = {
     # decode_split_kernel on the first 64 sequences of the decode-only batch:
-    # 2.290066 GB read + 5.18 MB written for 2.2576 GB algorithmic (x1.0167);
+    # 2.290050 GB read + 5.79 MB written for 2.2576 GB algorithmic (x1.0169);
     # scaled to the full batch by its algorithmic bytes (the KV read dominates
     # and grows in proportion).
-    "decode256_mha_d128": {"bytes": 9.374e9, "files": ["decode.cu", "common.cuh", "tc.cuh"],
-                           "src": "375942234a7586c8"},
+    "decode256_mha_d128": {"bytes": 9.376e9, "files": ["decode.cu", "common.cuh", "tc.cuh"],
+                           "src": "12f99537f959cf88"},
     # prefill_tc_kernel on the whole chunked-prefill workload (< 1 GB on the
-    # device, captured at full size): 706.78 MB read + 225.55 MB written.
-    "chunked_prefill_2x8192": {"bytes": 9.32339e8, "files": ["prefill_tc.cu", "common.cuh", "tc.cuh"],
-                               "src": "f26cb22ffcdc8c31"},
+    # device, captured at full size): 712.06 MB read + 224.71 MB written.
+    "chunked_prefill_2x8192": {"bytes": 9.36768e8, "files": ["prefill_tc.cu", "common.cuh", "tc.cuh"],
+                               "src": "ffa8d3f652f019c2"},
 }
 
 
@@ -375,28 +375,68 @@ def gpu_arm(args, wl):
     t_roof = max(alg["bytes"] / (peaks["hbm_gbs"] * 1e9), alg["flops"] / (peaks["bf16_tflops"] * 1e12))
     step_frac = t_roof / (ms_per_step / 1e3)
 
-    # ---- end to end through the C ABI from pinned host buffers
+    # ---- end to end through the C ABI from pinned host buffers.  Every step
+    # copies its qkv rows in from pinned host memory, uploads its metadata,
+    # runs the layer and copies its output rows back to pinned host memory.
+    # Steps are pipelined the way a serving loop would run them: copy-in,
+    # compute and copy-out on three streams over two device buffer sets (and
+    # two metadata objects, so a pinned staging buffer is never rewritten while
+    # its upload may still be pending), ordered by events.
     e2e = None
     if not args.no_e2e:
         with torch.cuda.stream(stream):
             qkv_host = qkv.cpu().pin_memory()
-            out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        E = max(3, min(K, 200))
-        for k in range(E + 2):
-            if k == 2:
-                stream.synchronize()
-                grp.barrier()
-                t0 = time.perf_counter()
+            out_host = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+            qkv_d = [qkv, torch.empty_like(qkv)]
+            out_d = [out, torch.empty_like(out)]
+            layers = [layer, R.RaggedLayer(params, wl.n_seqs, wl.n_tokens, nb_total, wl.max_len(), stream=stream)]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        ev_meta = [None, None]
+
+        def issue(k):
+            b = k % 2
+            with torch.cuda.stream(s_in):
+                if k >= 2:
+                    s_in.wait_event(ev_done[b])  # step k-2 no longer reads qkv_d[b]
+                qkv_d[b].copy_(qkv_host, non_blocking=True)
+                ev_in[b].record(s_in)
+            if ev_meta[b] is not None:
+                ev_meta[b].synchronize()  # step k-2's metadata upload left the staging buffer
             with torch.cuda.stream(stream):
-                qkv.copy_(qkv_host, non_blocking=True)
-                layer.build(descs, wl.num_blocks)
-                step()
-                out_host.copy_(out, non_blocking=True)
-            stream.synchronize()  # the result is on the host before the next step
+                stream.wait_event(ev_in[b])
+                if k >= 2:
+                    stream.wait_event(ev_out[b])  # step k-2's output is on the host
+                layers[b].build(descs, wl.num_blocks)
+                ev_meta[b] = torch.cuda.Event()
+                ev_meta[b].record(stream)
+                if fused:
+                    layers[b].fused(qkv_d[b], pool, out_d[b])
+                else:
+                    layers[b].append(qkv_d[b], pool)
+                    layers[b].attention(qkv_d[b], pool, out_d[b])
+                ev_done[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[b])
+                out_host[b].copy_(out_d[b], non_blocking=True)
+                ev_out[b].record(s_out)
+
+        E = max(3, min(K, 200))
+        for k in range(4):  # warm-up of the pipeline (both buffer sets)
+            issue(k)
+        torch.cuda.synchronize()
+        grp.barrier()
+        t0 = time.perf_counter()
+        for k in range(E):
+            issue(k)
+        torch.cuda.synchronize()  # every step's output is on the host
         e2e_s = grp.max(time.perf_counter() - t0, dev)
         e2e = {"value": ws * wl.n_tokens * E / e2e_s, "unit": "tokens/s",
                "h2d_bytes_per_step": int(qkv.numel() * qkv.element_size() + m.used_bytes),
-               "d2h_bytes_per_step": int(out.numel() * out.element_size()), "steps": E}
+               "d2h_bytes_per_step": int(out.numel() * out.element_size()), "steps": E,
+               "pipelined": "copy-in / compute / copy-out streams, 2 buffer sets"}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
