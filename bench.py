@@ -550,14 +550,18 @@ def component_multistep(args, wl):
     the layer, pass after pass; the workload's head shape, token budget 8192."""
     import torch
     from ragged_blocked_kv_raggedbatch_gb300 import ds_ragged as R
-    from ragged_blocked_kv_raggedbatch_gb300.splitfuse import SplitFusePlanner
+    from ragged_blocked_kv_raggedbatch_gb300.splitfuse import NativeSplitFusePlanner, SplitFusePlanner
     rng = np.random.default_rng(args.seed)
     prompts = np.floor(np.exp(rng.uniform(np.log(32), np.log(2048), 256))).astype(int)
     gens = rng.integers(16, 256, 256, endpoint=True)
     nblk = int(sum(-(-(p + g) // 64) for p, g in zip(prompts, gens))) + 64
     params = R.params_for(wl)
     alloc = R.BlockAllocator(nblk, rng.permutation(nblk))
-    plan = SplitFusePlanner(alloc, 8192, 256)
+    native = args.planner == "native"
+    if native:
+        plan = NativeSplitFusePlanner(alloc, 8192, 256, max_requests=256, max_blocks_per_request=64)
+    else:
+        plan = SplitFusePlanner(alloc, 8192, 256)
     for i in range(256):
         plan.add(i, int(prompts[i]), int(gens[i]))
     dt = W.torch_dtype(wl)
@@ -570,8 +574,13 @@ def component_multistep(args, wl):
     torch.cuda.synchronize()
     while not plan.idle:
         t0 = time.perf_counter()
-        batch = plan.next_batch()
-        descs = R.SeqDescs([b[1] for b in batch], [b[2] for b in batch], [b[3] for b in batch])
+        if native:
+            n = plan.plan()
+            descs = plan  # its ds_seq_desc[] goes to the metadata build as is
+            batch = None
+        else:
+            batch = plan.next_batch()
+            descs = R.SeqDescs([b[1] for b in batch], [b[2] for b in batch], [b[3] for b in batch])
         with torch.cuda.stream(st):
             layer.build(descs, nblk)
             host_s += time.perf_counter() - t0
@@ -581,14 +590,15 @@ def component_multistep(args, wl):
             layer.attention(qkv, pool, out)
             b.record(st)
         evs.append((a, b))
-        n = sum(x[2] for x in batch)
+        n = sum(plan.arr[i].new_tokens for i in range(plan.n)) if native else sum(x[2] for x in batch)
         toks += n
         passes += 1
         st.synchronize()  # the staging buffer is reused by the next pass
         plan.commit(batch)
     dev_s = sum(a.elapsed_time(b) for a, b in evs) / 1e3
     _line("splitfuse multi-pass new tokens/s per layer", toks / dev_s, "tokens/s",
-          {"workload": wl.name + "_heads", "requests": 256, "token_budget": 8192, "component": "multistep"},
+          {"workload": wl.name + "_heads", "requests": 256, "token_budget": 8192, "component": "multistep",
+           "planner": args.planner},
           passes=passes, tokens=toks, device_ms_per_pass=1e3 * dev_s / passes,
           host_us_per_pass=1e6 * host_s / passes, layer_launches=passes * 4)
 
@@ -656,6 +666,8 @@ def main(argv=None):
     ap.add_argument("--path", choices=["split", "fused"], default="split",
                     help="split: ds_kv_rotary_append then ds_blocked_attention; "
                          "fused: ds_fused_append_attention")
+    ap.add_argument("--planner", choices=["native", "python"], default="native",
+                    help="SplitFuse planner of the multistep component")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -396,6 +396,58 @@ ds_status ds_block_allocator_free(ds_block_allocator* a, const int32_t* ids, int
 ds_status ds_kv_blocks_required(int32_t seen_tokens, int32_t new_tokens, int32_t owned,
                                 int32_t block_size, int32_t* extra);
 
+/* ------------------------------------------------------ SplitFuse planner -- */
+
+/* Host-side Dynamic SplitFuse pass planner over the block ledger ("DeepSpeed-
+ * Inference and DeepSpeed-MII", tutorial ch. 10, sections 10.3 and 10.10:
+ * prefill chunks and single-token decodes merged into one batch under a token
+ * budget; "DeepSpeed Inference v2", section "The front desk": blocks are
+ * reserved from the allocator before a pass and returned when a sequence is
+ * flushed).  HOST memory only; no CUDA call; the state lives in caller memory
+ * of ds_splitfuse_mem_size bytes.
+ *
+ * A pass packs, in arrival order, one token for every request that has
+ * finished its prompt and still has tokens to generate, then prompt chunks
+ * of the requests still prefilling, until the token budget or max_seqs is
+ * reached.  A request whose extra blocks the ledger cannot supply waits for a
+ * later pass.  A request is done once its prompt is in the cache and
+ * `decode` decode passes have run; commit flushes it. */
+typedef struct ds_splitfuse {
+    void* mem;                      /* caller memory (8-byte aligned)           */
+    size_t mem_bytes;
+    int32_t max_requests;           /* requests tracked at once                 */
+    int32_t max_blocks_per_request; /* ceil((prompt + decode)/block_size) bound */
+    int32_t token_budget;           /* tokens per pass                          */
+    int32_t max_seqs;               /* sequences per pass                       */
+    int32_t block_size;
+    int32_t n_active;               /* requests not yet flushed                 */
+    int32_t n_planned;              /* sequences in the pass awaiting commit    */
+} ds_splitfuse;
+
+ds_status ds_splitfuse_mem_size(int32_t max_requests, int32_t max_blocks_per_request, size_t* bytes);
+/* Empty planner.  DS_ERR_INVALID_ARG on bad sizes or NULL memory,
+ * DS_ERR_WORKSPACE if mem_bytes is below ds_splitfuse_mem_size. */
+ds_status ds_splitfuse_init(ds_splitfuse* p, void* mem, size_t mem_bytes, int32_t max_requests,
+                            int32_t max_blocks_per_request, int32_t token_budget, int32_t max_seqs,
+                            int32_t block_size);
+/* Queue a request (prompt >= 1 tokens, then decode >= 0 generated tokens).
+ * DS_ERR_CAPACITY if max_requests are active or the request would need more
+ * than max_blocks_per_request blocks; DS_ERR_INVALID_ARG for bad counts or a
+ * uid that is already active. */
+ds_status ds_splitfuse_add(ds_splitfuse* p, int32_t uid, int32_t prompt, int32_t decode);
+/* Plan the next pass: reserves blocks from `alloc`, writes up to max_seqs
+ * descriptors to descs[] and their uids to uids[] (*n_out of them).
+ * descs[i].block_ids points into planner memory and stays valid until the
+ * next ds_splitfuse_commit.  DS_ERR_INVALID_ARG if the previous pass was not
+ * committed. */
+ds_status ds_splitfuse_next(ds_splitfuse* p, ds_block_allocator* alloc, ds_seq_desc* descs,
+                            int32_t* uids, int32_t* n_out);
+/* The planned pass ran: advance its sequences and flush the finished requests
+ * (their blocks go back to `alloc`; their uids, in arrival order, to
+ * flushed[] -- room for max_requests -- and *n_flushed). */
+ds_status ds_splitfuse_commit(ds_splitfuse* p, ds_block_allocator* alloc, int32_t* flushed,
+                              int32_t* n_flushed);
+
 /* Library version string. */
 const char* ds_version(void);
 

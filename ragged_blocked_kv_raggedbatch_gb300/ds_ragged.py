@@ -66,6 +66,12 @@ class ds_block_allocator(ctypes.Structure):
     _fields_ = [("stack", P), ("state", P), ("num_blocks", i32), ("n_free", i32)]
 
 
+class ds_splitfuse(ctypes.Structure):
+    _fields_ = [("mem", P), ("mem_bytes", ctypes.c_size_t), ("max_requests", i32),
+                ("max_blocks_per_request", i32), ("token_budget", i32), ("max_seqs", i32),
+                ("block_size", i32), ("n_active", i32), ("n_planned", i32)]
+
+
 # name -> (restype, argtypes); every entry point of include/ds_ragged.h
 SIGNATURES = {
     "ds_last_error": (ctypes.c_char_p, []),
@@ -87,6 +93,11 @@ SIGNATURES = {
     "ds_block_allocator_allocate": (i32, [P, i32, P]),
     "ds_block_allocator_free": (i32, [P, P, i32]),
     "ds_kv_blocks_required": (i32, [i32, i32, i32, i32, P]),
+    "ds_splitfuse_mem_size": (i32, [i32, i32, P]),
+    "ds_splitfuse_init": (i32, [P, P, ctypes.c_size_t, i32, i32, i32, i32, i32]),
+    "ds_splitfuse_add": (i32, [P, i32, i32, i32]),
+    "ds_splitfuse_next": (i32, [P, P, P, P, P]),
+    "ds_splitfuse_commit": (i32, [P, P, P, P]),
     "ds_kv_block_bytes": (i32, [P, P]),
     "ds_kv_offload": (i32, [P, P, P, i32, P, P]),
     "ds_kv_restore": (i32, [P, P, P, i32, P, P]),

@@ -12,7 +12,7 @@ import oracle
 from ragged_blocked_kv_raggedbatch_gb300 import build as B
 from ragged_blocked_kv_raggedbatch_gb300 import ds_ragged as R
 from ragged_blocked_kv_raggedbatch_gb300 import workloads as W
-from ragged_blocked_kv_raggedbatch_gb300.splitfuse import SplitFusePlanner
+from ragged_blocked_kv_raggedbatch_gb300.splitfuse import NativeSplitFusePlanner, SplitFusePlanner
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -115,6 +115,106 @@ def test_planner_invariants():
         assert tot[uid] == p + d
     assert alloc.n_free == 40 and plan.idle
     assert len(plan.freed) > 0
+
+
+def _drive(plan, alloc, stream, max_passes=10000):
+    """Feed (uid, prompt, decode, arrival pass) requests to a planner pass by
+    pass; returns the list of (batch, flushed) per pass and the final free count."""
+    log, k = [], 0
+    last = max(r[3] for r in stream)
+    while k < max_passes:
+        for uid, p, d, arr in stream:
+            if arr == k:
+                plan.add(uid, p, d)
+        if plan.idle and k > last:
+            break
+        batch = plan.next_batch()
+        flushed = plan.commit(batch)
+        log.append(([(u, s_, n, ids.tolist()) for u, s_, n, ids in batch], list(flushed)))
+        k += 1
+    return log, alloc.n_free
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_native_planner_matches_python_planner(case):
+    """ds_splitfuse_* makes the same passes as the Python planner, block for
+    block, on random request streams; tight pools make requests wait."""
+    rng = np.random.default_rng(100 + case)
+    n_req = int(rng.integers(5, 60))
+    budget = int(rng.choice([16, 64, 128, 512]))
+    max_seqs = int(rng.choice([2, 4, 16, 64]))
+    stream = [(int(1000 + i), int(rng.integers(1, 700)), int(rng.integers(0, 40)), int(rng.integers(0, 30)))
+              for i in range(n_req)]
+    need_max = max(-(-(p + d) // 64) for _, p, d, _ in stream)
+    num_blocks = int(max(need_max, rng.integers(need_max, 4 * need_max + 8)))
+    order = rng.permutation(num_blocks)
+    a_py = R.BlockAllocator(num_blocks, order)
+    a_nat = R.BlockAllocator(num_blocks, order)
+    py = SplitFusePlanner(a_py, budget, max_seqs)
+    nat = NativeSplitFusePlanner(a_nat, budget, max_seqs, max_requests=n_req, max_blocks_per_request=need_max)
+    log_py, free_py = _drive(py, a_py, stream)
+    log_nat, free_nat = _drive(nat, a_nat, stream)
+    assert log_nat == log_py
+    assert free_nat == free_py == num_blocks
+    assert nat.idle and py.idle
+    np.testing.assert_array_equal(a_nat.stack[: a_nat.n_free], a_py.stack[: a_py.n_free])
+
+
+def test_native_planner_descriptors_pack_like_copies():
+    """The planner's own ds_seq_desc[] (block lists in planner memory) packs to
+    the same metadata as descriptors built from copied block lists."""
+    rng = np.random.default_rng(7)
+    stream = [(i, int(rng.integers(1, 400)), int(rng.integers(0, 20)), 0) for i in range(12)]
+    alloc = R.BlockAllocator(200, rng.permutation(200))
+    nat = NativeSplitFusePlanner(alloc, 256, 8, max_requests=12, max_blocks_per_request=8)
+    for uid, p_, d, _ in stream:
+        nat.add(uid, p_, d)
+    params = R.make_params(4, 2, 64)
+    fake_dev = 1 << 40
+    for _ in range(30):
+        if nat.idle:
+            break
+        n = nat.plan()
+        copies = [(nat.arr[i].seen_tokens, nat.arr[i].new_tokens,
+                   np.ctypeslib.as_array(nat.arr[i].block_ids, shape=(nat.arr[i].n_blocks,)).copy())
+                  for i in range(n)]
+        metas = []
+        for descs in (nat, R.SeqDescs([c[0] for c in copies], [c[1] for c in copies], [c[2] for c in copies])):
+            dev, stg = R.ds_meta_buffer_sizes(8, 256, 64, params)
+            stage = np.zeros(stg // 4 + 4, np.int32)
+            meta = R.ds_ragged_meta()
+            meta.device_buf, meta.device_bytes = fake_dev, dev
+            meta.host_staging, meta.staging_bytes = stage.ctypes.data, stg
+            meta.max_seqs, meta.max_tokens, meta.max_blocks = 8, 256, 64
+            assert R.ds_ragged_meta_pack(descs, params, 200, meta) == R.DS_OK
+            metas.append(stage[: meta.used_bytes // 4].copy())
+        np.testing.assert_array_equal(metas[0], metas[1])
+        nat.commit()
+
+
+def test_native_planner_errors():
+    alloc = R.BlockAllocator(20)
+    nat = NativeSplitFusePlanner(alloc, 64, 4, max_requests=2, max_blocks_per_request=3)
+    lib = R.load()
+    assert lib.ds_splitfuse_add(R._ref(nat.p), 1, 0, 5) == R.DS_ERR_INVALID_ARG      # empty prompt
+    assert lib.ds_splitfuse_add(R._ref(nat.p), 1, 150, 50) == R.DS_ERR_CAPACITY      # 4 blocks > 3
+    nat.add(1, 100, 10)
+    assert lib.ds_splitfuse_add(R._ref(nat.p), 1, 10, 1) == R.DS_ERR_INVALID_ARG     # uid active
+    nat.add(2, 10, 1)
+    assert lib.ds_splitfuse_add(R._ref(nat.p), 3, 10, 1) == R.DS_ERR_CAPACITY        # 2 requests max
+    nat.plan()
+    n = np.zeros(1, np.int32)
+    descs = (R.ds_seq_desc * 4)()
+    uids = np.zeros(4, np.int32)
+    assert lib.ds_splitfuse_next(R._ref(nat.p), R._ref(alloc.a), R._ref(descs), uids.ctypes.data,
+                                 n.ctypes.data) == R.DS_ERR_INVALID_ARG            # not committed
+    nat.commit()
+    flushed = np.zeros(2, np.int32)
+    assert lib.ds_splitfuse_commit(R._ref(nat.p), R._ref(alloc.a), flushed.ctypes.data,
+                                   n.ctypes.data) == R.DS_ERR_INVALID_ARG          # nothing planned
+    small = np.zeros(4, np.uint64)
+    p2 = R.ds_splitfuse()
+    assert lib.ds_splitfuse_init(R._ref(p2), small.ctypes.data, small.nbytes, 2, 3, 64, 4, 64) == R.DS_ERR_WORKSPACE
 
 
 def _fields(heads=(4, 2), d=64, dtype="bf16"):
