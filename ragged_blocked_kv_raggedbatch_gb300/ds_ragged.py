@@ -355,7 +355,7 @@ class RaggedLayer:
     torch), plus the three calls of a forward pass."""
 
     def __init__(self, params: ds_attn_params, max_seqs: int, max_tokens: int, max_blocks: int,
-                 max_positions: int, device: str = "cuda", stream=None):
+                 max_positions: int, device: str = "cuda", stream=None, workspace=None):
         import torch
         self.params = params
         self.device = device
@@ -368,7 +368,8 @@ class RaggedLayer:
         self.rope_buf = torch.empty(max(rb, 16), dtype=torch.uint8, device=device)
         self.rope = ds_rope_table_build(params, max_positions, self.rope_buf, stream)
         wb = ds_blocked_attention_workspace_size(params, max_seqs, max_tokens, max_blocks)
-        self.workspace = torch.empty(wb, dtype=torch.uint8, device=device)
+        # a caller may share one workspace between layers whose calls are ordered on one stream
+        self.workspace = workspace if workspace is not None else torch.empty(wb, dtype=torch.uint8, device=device)
         self.fused_ws = None  # made (and its counters zeroed) on the first fused call
 
     def build(self, descs: SeqDescs, pool_num_blocks: int):
