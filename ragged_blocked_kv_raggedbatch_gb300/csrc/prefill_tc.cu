@@ -12,8 +12,8 @@
 // barrier phases and tensor memory carry over from one atom to the next.
 //
 // Roles (12 warps = 3 warpgroups; launched at 168 registers a thread, the
-// first warpgroup gives registers back (setmaxnreg 80) and the two softmax
-// warpgroups take them (setmaxnreg 208): 128*80 + 2*128*208 <= 384*168):
+// first warpgroup gives registers back (setmaxnreg 96) and the two softmax
+// warpgroups take them (setmaxnreg 200): 128*96 + 2*128*200 <= 384*168):
 //   warp 0      TMA producer: K and V tiles into 2-stage rings whose slots are
 //               freed separately (K after the last QK MMA that reads it, V after
 //               the last PV MMA), so each K tile is requested about a step and a
@@ -41,6 +41,18 @@
 #include <mutex>
 
 #include "tc.cuh"
+
+// Register split (per thread) between the producer/MMA warpgroup and the two
+// softmax warpgroups; 128 * LOW + 256 * HIGH must not exceed 384 * 168.
+// 96/200 is the split with no spill in any instance; on GB300 (chunked
+// prefill 2x8192, attention) 80/208 2.707 ms, 88/200 2.712-2.717, 96/200 2.703.
+#ifndef DSR_PF_REG_LOW
+#define DSR_PF_REG_LOW 96
+#endif
+#ifndef DSR_PF_REG_HIGH
+#define DSR_PF_REG_HIGH 200
+#endif
+static_assert(128 * DSR_PF_REG_LOW + 256 * DSR_PF_REG_HIGH <= 384 * 168, "register split over the launch budget");
 
 namespace dsr {
 
@@ -148,7 +160,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
   };
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(DSR_PF_REG_LOW) : "memory");
     if (warp == 0) {
       // ---------------------------------------------------------- producer
       const uint32_t box_tx = C::HALVES * C::BOX_BYTES;
@@ -322,7 +334,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
       tc::tmem_relinquish();
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;\n" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(DSR_PF_REG_HIGH) : "memory");
     // ------------------------------------------------------------ softmax
     const int x = (warp - 4) >> 2;            // 0: tile A, 1: tile B
     const int r = 32 * (warp & 3) + lane;     // row = tensor-memory lane
