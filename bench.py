@@ -46,15 +46,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # while the hash of the kernel's source files still matches the capture.
 NCU_TRAFFIC = {
     # decode_split_kernel on the first 64 sequences of the decode-only batch:
-    # 2.290050 GB read + 5.79 MB written for 2.2576 GB algorithmic (x1.0169);
+    # 2.290088 GB read + 5.80 MB written for 2.2576 GB algorithmic (x1.0170);
     # scaled to the full batch by its algorithmic bytes (the KV read dominates
     # and grows in proportion).
-    "decode256_mha_d128": {"bytes": 9.376e9, "files": ["decode.cu", "common.cuh", "tc.cuh"],
-                           "src": "12f99537f959cf88"},
+    "decode256_mha_d128": {"bytes": 9.377e9, "files": ["decode.cu", "common.cuh", "tc.cuh"],
+                           "src": "39cdb750be2dceba"},
     # prefill_tc_kernel on the whole chunked-prefill workload (< 1 GB on the
-    # device, captured at full size): 712.06 MB read + 224.71 MB written.
-    "chunked_prefill_2x8192": {"bytes": 9.36768e8, "files": ["prefill_tc.cu", "common.cuh", "tc.cuh"],
-                               "src": "ffa8d3f652f019c2"},
+    # device, captured at full size): 714.54 MB read + 224.78 MB written.
+    "chunked_prefill_2x8192": {"bytes": 9.39321e8, "files": ["prefill_tc.cu", "common.cuh", "tc.cuh"],
+                               "src": "7901a4bc70bb91be"},
 }
 
 
