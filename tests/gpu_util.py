@@ -31,7 +31,7 @@ def bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-class GpuRun:
+class LayerRun:
     """One forward pass of the layer on the GPU through the C ABI."""
 
     def __init__(self, wl, qkv, pool, rope_style=R.DS_ROPE_HALF, want_q=True, stream=None,
@@ -61,7 +61,7 @@ def check_out(wl, got: torch.Tensor, want: np.ndarray, where=""):
     return err.max(), err.mean()
 
 
-def full_check(wl, qkv, pool_before, run: GpuRun, pool_after):
+def full_check(wl, qkv, pool_before, run: LayerRun, pool_after):
     """Whole batch against the oracle (small batches)."""
     ref = oracle.layer(wl, qkv.cpu(), pool_before.cpu())
     meta = run.layer.read_meta()

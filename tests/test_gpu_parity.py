@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import GpuRun, bits, check_out, compact, full_check, sample_rows, ulp_diff
+from gpu_util import LayerRun, bits, check_out, compact, full_check, sample_rows, ulp_diff
 from ragged_blocked_kv_raggedbatch_gb300 import ds_ragged as R
 from ragged_blocked_kv_raggedbatch_gb300 import workloads as W
 
@@ -29,7 +29,7 @@ def _run_full(wl, rope_style=R.DS_ROPE_HALF, poison_unused=False):
         mask = keep.cuda()[:, None, None, :, None].expand(wl.pool_shape())
         pool.view(torch.int16).masked_fill_(~mask, -1)  # 0xFFFF: NaN in fp16 and bf16
     pool_before = pool.clone()
-    run = GpuRun(wl, qkv, pool, rope_style=rope_style)
+    run = LayerRun(wl, qkv, pool, rope_style=rope_style)
     if rope_style == R.DS_ROPE_HALF:
         return full_check(wl, qkv, pool_before, run, pool)
     # interleaved pairing: compare with the oracle's interleaved mode
@@ -84,7 +84,7 @@ def test_empty_batch_is_a_no_op():
     wl = W.make_custom([], 4, 2, 64, extra_blocks=2)
     qkv = torch.zeros((1, wl.qkv_width), dtype=torch.float16, device="cuda")
     pool = torch.zeros(wl.pool_shape(), dtype=torch.float16, device="cuda")
-    run = GpuRun(wl, qkv, pool)
+    run = LayerRun(wl, qkv, pool)
     assert run.dev_err == 0 and run.layer.meta.n_tokens == 0
     assert torch.isnan(run.out).all()  # nothing written
 
@@ -114,7 +114,7 @@ def test_full_size_sampled(name, seed):
     qkv, pool = W.make_values(wl, "cuda")
     seqs = _pick_sequences(wl, rng)
     sub, pool_c, qkv_c, gidx, old_ids = compact(wl, seqs, pool, qkv)
-    run = GpuRun(wl, qkv, pool, want_q=False)
+    run = LayerRun(wl, qkv, pool, want_q=False)
     assert run.dev_err == 0
     # metadata bit-exact against the oracle's for the whole batch
     meta = run.layer.read_meta()
@@ -149,14 +149,14 @@ def test_block_id_shuffle_is_bit_identical():
     wl = W.make_custom([(300, 50), (1000, 1), (64, 1), (0, 70)], 8, 2, 128, dtype="bf16", seed=5,
                        extra_blocks=4)
     qkv, pool = W.make_values(wl, "cuda")
-    a = GpuRun(wl, qkv, pool.clone(), want_q=False).out
+    a = LayerRun(wl, qkv, pool.clone(), want_q=False).out
     perm = np.random.default_rng(0).permutation(wl.num_blocks)
     pool2 = torch.empty_like(pool)
     pool2[torch.from_numpy(perm).cuda()] = pool
     wl2 = W.make_custom([(300, 50), (1000, 1), (64, 1), (0, 70)], 8, 2, 128, dtype="bf16", seed=5,
                         extra_blocks=4)
     wl2.block_ids = [perm[b].astype(np.int32) for b in wl.block_ids]
-    b = GpuRun(wl2, qkv, pool2, want_q=False).out
+    b = LayerRun(wl2, qkv, pool2, want_q=False).out
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
@@ -164,13 +164,13 @@ def test_sequence_order_permutes_rows():
     seqs = [(300, 50), (1000, 1), (64, 1), (0, 70), (129, 5)]
     wl = W.make_custom(seqs, 8, 2, 128, dtype="bf16", seed=6, extra_blocks=4)
     qkv, pool = W.make_values(wl, "cuda")
-    a = GpuRun(wl, qkv, pool.clone(), want_q=False).out
+    a = LayerRun(wl, qkv, pool.clone(), want_q=False).out
     order = [3, 1, 4, 0, 2]
     wl2 = W.subset(wl, order)
     cu = np.concatenate([[0], np.cumsum(wl.new)])
     gidx = np.concatenate([np.arange(cu[i], cu[i] + wl.new[i]) for i in order])
     qkv2 = qkv[torch.from_numpy(gidx).cuda()].contiguous()
-    b = GpuRun(wl2, qkv2, pool.clone(), want_q=False).out
+    b = LayerRun(wl2, qkv2, pool.clone(), want_q=False).out
     assert torch.equal(a[torch.from_numpy(gidx).cuda()].view(torch.int16), b.view(torch.int16))
 
 
@@ -179,7 +179,7 @@ def test_device_error_word_on_inconsistent_metadata():
     the kernels' bounds checks (error bit set, access skipped, no fault)."""
     wl = W.make_custom([(100, 3), (200, 1)], 4, 2, 64, dtype="fp16", seed=7, extra_blocks=2)
     qkv, pool = W.make_values(wl, "cuda")
-    run = GpuRun(wl, qkv, pool, want_q=False)
+    run = LayerRun(wl, qkv, pool, want_q=False)
     assert run.dev_err == 0
     layer = run.layer
     layer.build(run.descs, wl.num_blocks)  # re-pack into the pinned staging buffer
