@@ -83,7 +83,7 @@ typedef struct ds_seq_desc {
 } ds_seq_desc;
 
 /* Layer shape.  Supported: head_dim 64 or 128, block_size 64, n_q_heads a
- * multiple of n_kv_heads with g = n_q_heads/n_kv_heads in {1,2,4,8,16};
+ * multiple of n_kv_heads with g = n_q_heads/n_kv_heads in {1,2,4,8};
  * rope_theta > 0; softmax_scale <= 0 selects 1/sqrt(head_dim).
  * Query head h reads KV head floor(h / g). */
 typedef struct ds_attn_params {
