@@ -21,6 +21,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import subprocess
 import sys
@@ -43,26 +44,32 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
 # the dominant kernel from an ncu capture, keyed by workload; reported only
-# while the hash of the kernel's source files still matches the capture.
+# while the hash of the kernel's source files (comments and blank space
+# removed) still matches the capture.
 NCU_TRAFFIC = {
     # decode_split_kernel on the first 64 sequences of the decode-only batch:
     # 2.290088 GB read + 5.80 MB written for 2.2576 GB algorithmic (x1.0170);
     # scaled to the full batch by its algorithmic bytes (the KV read dominates
     # and grows in proportion).
     "decode256_mha_d128": {"bytes": 9.377e9, "files": ["decode.cu", "common.cuh", "tc.cuh"],
-                           "src": "39cdb750be2dceba"},
+                           "src": "6f868d52f8c764c0"},
     # prefill_tc_kernel on the whole chunked-prefill workload (< 1 GB on the
     # device, captured at full size): 714.54 MB read + 224.78 MB written.
     "chunked_prefill_2x8192": {"bytes": 9.39321e8, "files": ["prefill_tc.cu", "common.cuh", "tc.cuh"],
-                               "src": "7901a4bc70bb91be"},
+                               "src": "dcb73b12bc171f53"},
 }
 
 
 def _src_hash(files) -> str:
+    """Hash of the kernel's source files with comments and blank space
+    removed, so that editing a comment does not invalidate a capture."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ragged_blocked_kv_raggedbatch_gb300", "csrc")
     for f in files:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        text = open(os.path.join(csrc, f), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

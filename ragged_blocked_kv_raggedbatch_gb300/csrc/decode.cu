@@ -32,7 +32,9 @@
 // tile pair, 32 KB at D=128) and CTAs per SM the registers must allow, for
 // G < 4 and G >= 4 query heads per KV head.  Measured on GB300 (decode rows of
 // the 2048-token SplitFuse batch, G=4): 4 warps x 2 stages x 3 CTAs/SM
-// 6.52 TB/s; 4 x 3 x 2: 5.63; 8 x 2 x 2: 5.35; 8 x 3 x 1: 3.69.
+// 6.52 TB/s; 4 x 3 x 2: 5.63; 8 x 2 x 2: 5.35; 8 x 3 x 1: 3.69.  G=1 (256
+// decode rows, attention call): 4 x 2 x 3 1.2692 ms; 8 x 2 x 3 1.2681;
+// 8 x 3 x 2 1.2732; 4 x 3 x 2 1.2761; 2 x 2 x 3 1.2784; 2 x 3 x 2 1.2905.
 #ifndef DSR_DECODE_WARPS
 #define DSR_DECODE_WARPS 4
 #endif
