@@ -344,6 +344,32 @@ def gpu_arm(args, wl):
                     flush.zero_()
         stream.synchronize()
     clocks = clk.summary()
+    # the same steps with L2 flushed before each one (a 512 MB write, untimed),
+    # next to the main loop's (which flushes only when a step's bytes are
+    # below twice L2)
+    flushed = None
+    if flush is None:
+        fl = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+        K2 = max(3, min(K, 50))
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
+        with torch.cuda.stream(stream):
+            for k in range(K2):
+                fl.zero_()
+                a, b, c = ev2[k]
+                a.record(stream)
+                if fused:
+                    b.record(stream)
+                    layer.fused(qkv, pool, out)
+                else:
+                    layer.append(qkv, pool)
+                    b.record(stream)
+                    layer.attention(qkv, pool, out)
+                c.record(stream)
+        stream.synchronize()
+        flushed = {"ms_per_step": float(np.mean([a.elapsed_time(c) for a, b, c in ev2])),
+                   "attention_ms": float(np.mean([b.elapsed_time(c) for a, b, c in ev2])), "steps": K2}
+        del fl
     step_ms = [a.elapsed_time(c) for a, b, c in ev]
     attn_ms = [b.elapsed_time(c) for a, b, c in ev]
     app_ms = [a.elapsed_time(b) for a, b, c in ev]
@@ -468,6 +494,13 @@ def gpu_arm(args, wl):
             "algorithmic": {"flops": alg["flops"], "bytes": alg["bytes"]},
             "hbm_frac_vs_8tbs": (alg["attn_bytes"] / attn_mean_s / 1e9) / 8000.0,
             "meta_build_us": meta_build_us,
+            "l2_flushed": flushed,
+            # bytes the implementation moves: the append (K, V read and written),
+            # the attention call (Q, every KV row incl. the new ones, O, block
+            # ids) and the split-K partials (written, then read by the merge)
+            "workspace_bytes": int(m.n_decode_items * wl.n_q_heads * (wl.head_dim + 2) * 4),
+            "implemented_bytes": int(alg["append_bytes"] + alg["attn_bytes"] +
+                                     2 * m.n_decode_items * wl.n_q_heads * (wl.head_dim + 2) * 4),
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches_per_step * K,
             "clocks": clocks,
         }
