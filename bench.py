@@ -220,6 +220,21 @@ def time_oracle(wl, seconds: float = 12.0, seed: int = 0):
     return rows / dt, threads, desc, dt
 
 
+def _l2_note(wl) -> str:
+    step_bytes = algorithmic(wl)["bytes"]
+    return ("inputs larger than L2 (%.2f GB per step)" % (step_bytes / 1e9) if step_bytes >= 2 * L2_BYTES
+            else "L2 flushed between timed steps (512 MB write, untimed)")
+
+
+def run_config(wl, args, world: int) -> dict:
+    """The workload's config object, the same on both arms' lines."""
+    return {"workload": wl.name, "n_seqs": wl.n_seqs, "new_tokens": wl.n_tokens,
+            "kv_history_tokens": int(wl.seen.sum()), "n_q_heads": wl.n_q_heads,
+            "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim, "block_size": 64,
+            "rope_theta": wl.rope_theta, "seed": wl.seed, "l2": _l2_note(wl),
+            "path": args.path, "parallelism": "replicas" if world > 1 else "single"}
+
+
 def reference_arm(args, wl):
     ws, rank, _ = replicas.env()
     if rank != 0:
@@ -255,10 +270,11 @@ def reference_arm(args, wl):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / max(1, len(times)), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "rows_per_step": samples[0][0].n_tokens},
+        "config": run_config(wl, args, ws),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": "about %d rows per step sampled from %s (fresh values, same "
-                                   "distribution; 4 samples reused)" % (rows, wl.name)},
+                         "sample": "about %d rows per step (%d in the first sample) drawn from %s "
+                                   "(fresh values, same distribution; 4 samples reused)"
+                                   % (rows, samples[0][0].n_tokens, wl.name)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -313,8 +329,6 @@ def gpu_arm(args, wl):
     step_bytes = alg["bytes"]
     if step_bytes < 2 * L2_BYTES:
         flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
-    l2_note = ("inputs larger than L2 (%.2f GB per step)" % (step_bytes / 1e9) if flush is None
-               else "L2 flushed between timed steps (512 MB write, untimed)")
 
     for _ in range(args.warmup):
         step()
@@ -482,11 +496,7 @@ def gpu_arm(args, wl):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-            "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "new_tokens": wl.n_tokens,
-                       "kv_history_tokens": int(wl.seen.sum()), "n_q_heads": wl.n_q_heads,
-                       "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim, "block_size": 64,
-                       "rope_theta": wl.rope_theta, "seed": wl.seed, "l2": l2_note,
-                       "path": args.path, "parallelism": "replicas" if ws > 1 else "single"},
+            "config": run_config(wl, args, ws),
             "roofline": roof,
             "step_roofline_frac": step_frac,
             "decode_kv_gbps": alg["kv_history_bytes"] / (float(np.mean(attn_ms)) / 1e3) / 1e9,
