@@ -341,10 +341,14 @@ ds_status ds_ragged_meta_pack(const ds_seq_desc* seqs, int32_t n_seqs,
   m->split_blocks = split;
   // SMs for the persistent prefill grid when decode rows run beside it: enough
   // for the prefill atoms to finish well within the time the decode rows take
-  // to stream their KV history.  Costs measured on GB300: ~1.8 us per 128-key
-  // step of a two-tile atom (1.2 us with one tile); decode KV at ~6.4 TB/s.
-  // The margin (DSR_PREFILL_SM_FACTOR) was swept on GB300: SplitFuse 2048 at
-  // 1.0 / 1.25 / 1.6 / 2.2: 2.08 / 1.79 / 1.59 / 1.35 ms.
+  // to stream their KV history.  Costs measured on GB300 with the first
+  // persistent kernel: ~1.8 us per 128-key step of a two-tile atom (1.2 us
+  // with one tile); decode KV at ~6.4 TB/s.  The margin (DSR_PREFILL_SM_FACTOR)
+  // was swept on GB300: SplitFuse 2048 at 1.0 / 1.25 / 1.6 / 2.2: 2.08 / 1.79 /
+  // 1.59 / 1.35 ms.  With the faster prefill kernel (~1.4 us per two-tile step)
+  // the share matters little above 1.6: SplitFuse 1.6 / 2.2 / 3.0 / all SMs
+  // 1.357 / 1.357 / 1.354 / 1.349 ms, max ragged within 1.5 % from 1.2 to all
+  // SMs (its decode CTAs take as long on few SMs as on many).
   m->prefill_sms = 0.f;
   if (!tv.empty() && dec_blocks > 0) {
     double pre_us = 0.0;
