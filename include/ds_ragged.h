@@ -439,7 +439,9 @@ ds_status ds_splitfuse_add(ds_splitfuse* p, int32_t uid, int32_t prompt, int32_t
  * descriptors to descs[] and their uids to uids[] (*n_out of them).
  * descs[i].block_ids points into planner memory and stays valid until the
  * next ds_splitfuse_commit.  DS_ERR_INVALID_ARG if the previous pass was not
- * committed. */
+ * committed.  When the ledger cannot supply any request's blocks the pass is
+ * empty (*n_out == 0) while requests stay active; the caller frees blocks
+ * (or stops) before planning again. */
 ds_status ds_splitfuse_next(ds_splitfuse* p, ds_block_allocator* alloc, ds_seq_desc* descs,
                             int32_t* uids, int32_t* n_out);
 /* The planned pass ran: advance its sequences and flush the finished requests
