@@ -614,6 +614,7 @@ def component_multistep(args, wl):
     params = R.params_for(wl)
     alloc = R.BlockAllocator(nblk, rng.permutation(nblk))
     native = args.planner == "native"
+    fused = args.path == "fused"
     if native:
         plan = NativeSplitFusePlanner(alloc, 8192, 256, max_requests=256, max_blocks_per_request=64)
     else:
@@ -640,8 +641,11 @@ def component_multistep(args, wl):
         with torch.cuda.stream(st):
             layer.build(descs, nblk)
             host_s += time.perf_counter() - t0
-            layer.append(qkv, pool)
-            layer.attention(qkv, pool, out)
+            if fused:
+                layer.fused(qkv, pool, out)
+            else:
+                layer.append(qkv, pool)
+                layer.attention(qkv, pool, out)
         st.synchronize()
         # keep a copy of the pass for the replay below (bench bookkeeping, not timed)
         tr = time.perf_counter()
@@ -660,12 +664,15 @@ def component_multistep(args, wl):
     wall_s = time.perf_counter() - t_wall - rec_s
     passes = len(recorded)
 
-    # device rate: replay the recorded passes back to back
-    ws_t = layer.workspace
+    # device rate: replay the recorded passes back to back (one shared
+    # workspace; the fused path's counters are back at zero after each call)
+    ws_t = layer.fused_ws if fused else layer.workspace
     layers = []
     with torch.cuda.stream(st):
         for rec in recorded:
             L = R.RaggedLayer(params, 256, 8192, nblk, 4096, stream=st, workspace=ws_t)
+            if fused:
+                L.fused_ws = ws_t
             L.build(R.SeqDescs([r[0] for r in rec], [r[1] for r in rec], [r[2] for r in rec]), nblk)
             layers.append(L)
     st.synchronize()
@@ -676,15 +683,18 @@ def component_multistep(args, wl):
             torch.cuda._sleep(20_000_000)  # the host enqueues every pass before the GPU reaches them
             a.record(st)
             for L in layers:
-                L.append(qkv, pool)
-                L.attention(qkv, pool, out)
+                if fused:
+                    L.fused(qkv, pool, out)
+                else:
+                    L.append(qkv, pool)
+                    L.attention(qkv, pool, out)
             b.record(st)
         st.synchronize()
         rep.append(a.elapsed_time(b) / 1e3)
     dev_s = float(np.median(rep))
     _line("splitfuse multi-pass new tokens/s per layer", toks / dev_s, "tokens/s",
           {"workload": wl.name + "_heads", "requests": 256, "token_budget": 8192, "component": "multistep",
-           "planner": args.planner},
+           "planner": args.planner, "path": args.path},
           passes=passes, tokens=toks, device_ms_per_pass=1e3 * dev_s / passes,
           live_wall_us_per_pass=1e6 * wall_s / passes, live_tokens_per_s=toks / wall_s,
           host_us_per_pass=1e6 * host_s / passes, layer_launches_per_pass=4)
