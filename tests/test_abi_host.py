@@ -109,13 +109,19 @@ def _check_coverage(wl, meta, got):
         assert seq == dec[k] and tok == got["cu_seqlens"][seq]
         nb = -(-(int(wl.seen[seq]) + 1) // 64)
         blocks = []
-        for it in got["decode_items"][first:first + cnt]:
-            assert it[0] == seq and it[2] - it[1] <= meta.split_blocks
+        split = meta.split_blocks
+        # what the fused decode kernel's in-kernel merge derives from one item:
+        # the row's split count and its first partial slot
+        assert cnt == -(-nb // split)
+        for k, it in enumerate(got["decode_items"][first:first + cnt]):
+            assert it[0] == seq and it[2] - it[1] <= split
+            assert it[1] == k * split
             blocks += list(range(it[1], it[2]))
             if cnt == 1:
                 assert it[3] == -1
             else:
                 slots.append(int(it[3]))
+                assert it[3] - it[1] // split == got["decode_items"][first][3]
         assert blocks == list(range(nb))
     assert len(slots) == len(set(slots))
     assert len(got["decode_items"]) == meta.n_decode_items
