@@ -446,7 +446,10 @@ ds_status ds_splitfuse_next(ds_splitfuse* p, ds_block_allocator* alloc, ds_seq_d
                             int32_t* uids, int32_t* n_out);
 /* The planned pass ran: advance its sequences and flush the finished requests
  * (their blocks go back to `alloc`; their uids, in arrival order, to
- * flushed[] -- room for max_requests -- and *n_flushed). */
+ * flushed[] -- room for max_requests -- and *n_flushed).  If the ledger
+ * rejects a returned block (it no longer matches this planner: another party
+ * freed or re-used the block), the ledger's status is returned and the
+ * planner must be initialised again. */
 ds_status ds_splitfuse_commit(ds_splitfuse* p, ds_block_allocator* alloc, int32_t* flushed,
                               int32_t* n_flushed);
 
