@@ -82,6 +82,36 @@ def test_pack_matches_oracle_bit_exact(lib, name):
     _check_coverage(wl, pk.meta, got)
 
 
+@pytest.mark.parametrize("case", range(40))
+def test_pack_random_batches_bit_exact(lib, case):
+    """Random ragged batches (mixes of first tokens, decodes and chunks that
+    cross block boundaries; any head ratio and head size; spare pool blocks;
+    capacities with slack) pack to the oracle's metadata and a covering work
+    list."""
+    rng = np.random.default_rng(7000 + case)
+    n = int(rng.integers(1, 40))
+    seqs = []
+    for _ in range(n):
+        kind = rng.integers(0, 4)
+        seen = int(rng.choice([0, rng.integers(0, 64), rng.integers(0, 5000)]))
+        new = 1 if kind < 2 else int(rng.integers(1, 600))
+        seqs.append((seen, new))
+    hkv = int(rng.choice([1, 2, 4, 8]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    d = int(rng.choice([64, 128]))
+    wl = W.make_custom(seqs, hkv * g, hkv, d, dtype=str(rng.choice(["bf16", "fp16"])), seed=case,
+                       extra_blocks=int(rng.integers(0, 20)))
+    nb = int(wl.blocks_needed().sum())
+    pk = Packed(wl, max_seqs=wl.n_seqs + int(rng.integers(0, 5)), max_tokens=wl.n_tokens + int(rng.integers(0, 50)),
+                max_blocks=nb + int(rng.integers(0, 30)))
+    assert pk.pack() == R.DS_OK, lib.ds_last_error()
+    got = pk.arrays()
+    want = oracle.meta_build(wl)
+    for key in ["cu_seqlens", "seq_seen", "seq_new", "blk_off", "block_table", "tok_seq", "tok_pos"]:
+        np.testing.assert_array_equal(got[key], want[key], err_msg=key)
+    _check_coverage(wl, pk.meta, got)
+
+
 def _check_coverage(wl, meta, got):
     """Every prefill token is covered by exactly one tile; every KV block of
     every decode row by exactly one split item; slots are unique."""
