@@ -61,9 +61,10 @@ def check_out(wl, got: torch.Tensor, want: np.ndarray, where=""):
     return err.max(), err.mean()
 
 
-def full_check(wl, qkv, pool_before, run: LayerRun, pool_after):
-    """Whole batch against the oracle (small batches)."""
-    ref = oracle.layer(wl, qkv.cpu(), pool_before.cpu())
+def full_check(wl, qkv, pool_before, run: LayerRun, pool_after, style: int = R.DS_ROPE_HALF):
+    """Whole batch against the oracle (small batches); `style` is the rotary
+    pairing the run used (the oracle's constants have the same values)."""
+    ref = oracle.layer(wl, qkv.cpu(), pool_before.cpu(), style=style)
     meta = run.layer.read_meta()
     for key in ["cu_seqlens", "seq_seen", "seq_new", "blk_off", "block_table", "tok_seq", "tok_pos"]:
         np.testing.assert_array_equal(meta[key], ref["meta"][key], err_msg=key)
