@@ -308,6 +308,24 @@ def test_fused_call_validation_before_launch(lib):
     assert init(None, fused.value) == R.DS_ERR_INVALID_ARG
 
 
+def test_empty_batch_calls_enqueue_nothing(lib):
+    """A batch with no sequences packs, and the layer calls return DS_OK
+    before any CUDA call (so they are safe on a host without a GPU)."""
+    wl = W.make_custom([], 4, 2, 64)
+    pk = Packed(wl, max_seqs=1, max_tokens=1, max_blocks=1, pool_blocks=4)
+    assert pk.pack() == R.DS_OK
+    assert pk.meta.n_tokens == 0 and pk.meta.n_decode_items == 0 and pk.meta.n_prefill_tiles == 0
+    p = pk.params
+    rope = R.ds_rope_table(FAKE_DEV, 1, 64, float(wl.rope_theta))
+    pool = R.ds_kv_pool(FAKE_DEV, 4)
+    assert lib.ds_kv_rotary_append(R._ref(pk.meta), R._ref(p), R._ref(rope), FAKE_DEV, None,
+                                   R._ref(pool), None) == R.DS_OK
+    assert lib.ds_blocked_attention(R._ref(pk.meta), R._ref(p), R._ref(rope), FAKE_DEV, R._ref(pool),
+                                    FAKE_DEV, None, 0, None) == R.DS_OK
+    assert lib.ds_fused_append_attention(R._ref(pk.meta), R._ref(p), R._ref(rope), FAKE_DEV, R._ref(pool),
+                                         FAKE_DEV, None, 0, None) == R.DS_OK
+
+
 def test_offload_restore_and_gather_validation(lib):
     """Argument errors of the data-movement calls are found on the host."""
     p = R.make_params(8, 2, 128)
