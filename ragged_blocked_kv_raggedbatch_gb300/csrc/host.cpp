@@ -225,18 +225,23 @@ ds_status ds_ragged_meta_pack(const ds_seq_desc* seqs, int32_t n_seqs,
   if (B > m->max_blocks)
     return fail(DS_ERR_CAPACITY, "%lld block-table entries exceed max_blocks %d", (long long)B,
                 m->max_blocks);
-  // Block ids: inside the pool and never shared inside one batch.
-  std::vector<uint8_t> used((size_t)pool_num_blocks, 0);
+  // Block ids: inside the pool and never shared inside one batch (one bit
+  // per pool block, in a buffer kept per thread; ~1 ns per id).
+  thread_local std::vector<uint64_t> used;
+  used.assign(((size_t)pool_num_blocks + 63) / 64, 0);
+  uint64_t* const bits = used.data();  // one lookup of the thread-local buffer
   for (int32_t i = 0; i < n_seqs; ++i) {
     const ds_seq_desc& d = seqs[i];
-    int64_t nb = ((int64_t)d.seen_tokens + d.new_tokens + bs - 1) / bs;
+    const int64_t nb = ((int64_t)d.seen_tokens + d.new_tokens + bs - 1) / bs;
+    const int32_t* ids = d.block_ids;
     for (int64_t b = 0; b < nb; ++b) {
-      int32_t id = d.block_ids[b];
-      if (id < 0 || id >= pool_num_blocks)
+      const int32_t id = ids[b];
+      if ((uint32_t)id >= (uint32_t)pool_num_blocks)
         return fail(DS_ERR_BAD_BLOCK, "sequence %d block %lld: id %d outside pool of %d", i,
                     (long long)b, id, pool_num_blocks);
-      if (used[id]) return fail(DS_ERR_BAD_BLOCK, "block id %d used twice in the batch", id);
-      used[id] = 1;
+      const uint64_t bit = (uint64_t)1 << (id & 63);
+      if (bits[(size_t)id >> 6] & bit) return fail(DS_ERR_BAD_BLOCK, "block id %d used twice in the batch", id);
+      bits[(size_t)id >> 6] |= bit;
     }
   }
 
@@ -258,7 +263,10 @@ ds_status ds_ragged_meta_pack(const ds_seq_desc* seqs, int32_t n_seqs,
 
   Layout L = layout_for(n_seqs, N, B, pre_tiles, n_items, n_dec);
   int32_t* w = static_cast<int32_t*>(m->host_staging);
-  std::memset(w, 0, L.total * 4);
+  // Every region below is written in full; only the header and the alignment
+  // words before the work lists need clearing.
+  std::memset(w + L.hdr, 0, dsr::HDR_WORDS * 4);
+  std::memset(w + L.tpos + N, 0, (L.tiles - (L.tpos + N)) * 4);
   w[L.hdr + dsr::HDR_ERR] = 0;
   w[L.hdr + dsr::HDR_S] = n_seqs;
   w[L.hdr + dsr::HDR_N] = (int32_t)N;

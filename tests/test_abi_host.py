@@ -112,6 +112,20 @@ def test_pack_random_batches_bit_exact(lib, case):
     _check_coverage(wl, pk.meta, got)
 
 
+@pytest.mark.parametrize("name", ["tiny_gqa_d64", "splitfuse2048_gqa_d128", "max_ragged_8192"])
+def test_pack_writes_every_uploaded_word(lib, name):
+    """The packed image is the same whatever the staging buffer held before:
+    every word up to used_bytes is written (or zeroed) by the pack."""
+    wl = W.make_workload(name, 0)
+    images = []
+    for fill in (0, -0x54545455):  # zeros, then a 0xABABABAB pattern
+        pk = Packed(wl)
+        pk.stage[:] = fill
+        assert pk.pack() == R.DS_OK
+        images.append(pk.stage[: pk.meta.used_bytes // 4].copy())
+    np.testing.assert_array_equal(images[0], images[1])
+
+
 def _check_coverage(wl, meta, got):
     """Every prefill token is covered by exactly one tile; every KV block of
     every decode row by exactly one split item; slots are unique."""
