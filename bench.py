@@ -606,19 +606,15 @@ def component_multistep(args, wl):
     beforehand, so the GPU never waits for the host."""
     import torch
     from ragged_blocked_kv_raggedbatch_gb300 import ds_ragged as R
-    from ragged_blocked_kv_raggedbatch_gb300.splitfuse import NativeSplitFusePlanner, SplitFusePlanner
+    from ragged_blocked_kv_raggedbatch_gb300.splitfuse import NativeSplitFusePlanner
     rng = np.random.default_rng(args.seed)
     prompts = np.floor(np.exp(rng.uniform(np.log(32), np.log(2048), 256))).astype(int)
     gens = rng.integers(16, 256, 256, endpoint=True)
     nblk = int(sum(-(-(p + g) // 64) for p, g in zip(prompts, gens))) + 64
     params = R.params_for(wl)
     alloc = R.BlockAllocator(nblk, rng.permutation(nblk))
-    native = args.planner == "native"
     fused = args.path == "fused"
-    if native:
-        plan = NativeSplitFusePlanner(alloc, 8192, 256, max_requests=256, max_blocks_per_request=64)
-    else:
-        plan = SplitFusePlanner(alloc, 8192, 256)
+    plan = NativeSplitFusePlanner(alloc, 8192, 256, max_requests=256, max_blocks_per_request=64)
     for i in range(256):
         plan.add(i, int(prompts[i]), int(gens[i]))
     dt = W.torch_dtype(wl)
@@ -632,12 +628,8 @@ def component_multistep(args, wl):
     t_wall = time.perf_counter()
     while not plan.idle:
         t0 = time.perf_counter()
-        if native:
-            n = plan.plan()
-            descs = plan  # its ds_seq_desc[] goes to the metadata build as is
-        else:
-            batch = plan.next_batch()
-            descs = R.SeqDescs([b[1] for b in batch], [b[2] for b in batch], [b[3] for b in batch])
+        n = plan.plan()
+        descs = plan  # its ds_seq_desc[] goes to the metadata build as is
         with torch.cuda.stream(st):
             layer.build(descs, nblk)
             host_s += time.perf_counter() - t0
@@ -649,17 +641,14 @@ def component_multistep(args, wl):
         st.synchronize()
         # keep a copy of the pass for the replay below (bench bookkeeping, not timed)
         tr = time.perf_counter()
-        if native:
-            rec = [(plan.arr[i].seen_tokens, plan.arr[i].new_tokens,
-                    np.ctypeslib.as_array(plan.arr[i].block_ids, shape=(plan.arr[i].n_blocks,)).copy())
-                   for i in range(n)]
-        else:
-            rec = [(b[1], b[2], b[3]) for b in batch]
+        rec = [(plan.arr[i].seen_tokens, plan.arr[i].new_tokens,
+                np.ctypeslib.as_array(plan.arr[i].block_ids, shape=(plan.arr[i].n_blocks,)).copy())
+               for i in range(n)]
         recorded.append(rec)
         toks += sum(r[1] for r in rec)
         t1 = time.perf_counter()
         rec_s += t1 - tr
-        plan.commit(None if native else batch)
+        plan.commit()
         host_s += time.perf_counter() - t1
     wall_s = time.perf_counter() - t_wall - rec_s
     passes = len(recorded)
@@ -694,7 +683,7 @@ def component_multistep(args, wl):
     dev_s = float(np.median(rep))
     _line("splitfuse multi-pass new tokens/s per layer", toks / dev_s, "tokens/s",
           {"workload": wl.name + "_heads", "requests": 256, "token_budget": 8192, "component": "multistep",
-           "planner": args.planner, "path": args.path},
+           "planner": "native", "path": args.path},
           passes=passes, tokens=toks, device_ms_per_pass=1e3 * dev_s / passes,
           live_wall_us_per_pass=1e6 * wall_s / passes, live_tokens_per_s=toks / wall_s,
           host_us_per_pass=1e6 * host_s / passes, layer_launches_per_pass=4)
@@ -763,8 +752,6 @@ def main(argv=None):
     ap.add_argument("--path", choices=["split", "fused"], default="split",
                     help="split: ds_kv_rotary_append then ds_blocked_attention; "
                          "fused: ds_fused_append_attention")
-    ap.add_argument("--planner", choices=["native", "python"], default="native",
-                    help="SplitFuse planner of the multistep component")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

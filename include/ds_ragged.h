@@ -219,7 +219,8 @@ ds_status ds_kv_rotary_append(const ds_ragged_meta* meta, const ds_attn_params* 
                               const ds_kv_pool* pool, void* stream);
 
 /* Workspace bytes ds_blocked_attention needs for any batch within the
- * capacities (decode split partials). */
+ * capacities (decode split partials: fp32 (m, l) pairs per item and query
+ * head, then the fp32 o vectors from the next 256-byte boundary). */
 ds_status ds_blocked_attention_workspace_size(const ds_attn_params* params, int32_t max_seqs,
                                               int32_t max_tokens, int32_t max_blocks,
                                               size_t* bytes);
@@ -297,12 +298,16 @@ ds_status ds_fused_append_attention(const ds_ragged_meta* meta, const ds_attn_pa
  * Limits and behaviour:
  *  - The scratch array is DS_STATIC_WORKSPACE_BYTES (32 MiB) of device memory,
  *    held on every GPU that loads the library until the process exits.  A
- *    batch whose split partials need more (n_decode_items * n_q_heads *
- *    (head_dim + 2) * 4 bytes) is rejected with DS_ERR_WORKSPACE before
+ *    batch whose split partials need more (4 * (P + n_decode_items *
+ *    n_q_heads * head_dim) bytes, P = 2 * n_decode_items * n_q_heads rounded
+ *    up to a multiple of 64) is rejected with DS_ERR_WORKSPACE before
  *    anything is enqueued.
  *  - The first call on each device (with that device current) looks up the
  *    array's device address once; make that first call before any stream
- *    capture begins.
+ *    capture begins.  The address stays cached for the life of the process:
+ *    after cudaDeviceReset (or anything else that destroys and re-creates
+ *    the device's primary context) it is stale, so do not call this entry
+ *    point again in that process.
  *  - Every call on a device shares the one array, which keeps the last call's
  *    contents.  Nothing in it has to start at zero (every partial is written
  *    before it is read), so it is never cleared.  Calls whose work overlaps

@@ -27,6 +27,17 @@ constexpr int kPrefillRows = 256;     // rows (tokens x heads of one KV group) p
 constexpr int kMinSplitBlocks = 4;    // smallest decode split, in KV blocks
 constexpr int kMaxSplitBlocks = 32;   // largest decode split, in KV blocks
 
+// Split-decode partials in a workspace: the (m, l) pairs [items][Hq][2],
+// then o [items][Hq][D] from the next 256-byte boundary, so that the float4
+// accesses to o stay 16-byte aligned for any item and head count.
+__host__ __device__ constexpr int64_t ws_o_offset(int64_t n_items, int64_t Hq) {
+  return (n_items * Hq * 2 + 63) / 64 * 64;
+}
+// Bytes of the partials of n_items split items.
+__host__ __device__ constexpr int64_t ws_partial_bytes(int64_t n_items, int64_t Hq, int64_t D) {
+  return (ws_o_offset(n_items, Hq) + n_items * Hq * D) * 4;
+}
+
 // Kernel arguments that every launch needs, resolved on the host.
 struct LayerArgs {
   int32_t Hq, Hkv, D, G, dtype, style;

@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 4 ? DSR_DECODE_MINB_GQA : DSR
       *reinterpret_cast<uint4*>(out + (int64_t)t * a.Hq * D + hq * D + 8 * d8) = pk;
     } else {
       float* wml = ws + ((int64_t)slot * a.Hq + hq) * 2;
-      float* wo = ws + (int64_t)n_items * a.Hq * 2 + ((int64_t)slot * a.Hq + hq) * D + 8 * d8;
+      float* wo = ws + ws_o_offset(n_items, a.Hq) + ((int64_t)slot * a.Hq + hq) * D + 8 * d8;
       if (d8 == 0) {
         wml[0] = M;
         wml[1] = lsum;
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 4 ? DSR_DECODE_MINB_GQA : DSR
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    const float* wo_base = ws + (int64_t)n_items * a.Hq * 2;
+    const float* wo_base = ws + ws_o_offset(n_items, a.Hq);
     for (int u = tid; u < units; u += WARPS * 32) {
       const int h = u / (D / 8), d8 = u % (D / 8);
       const int hq = c * G + h;
@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const int4* __restr
 #pragma unroll
   for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
   float lsum = 0.f;
-  const float* wo = ws + (int64_t)n_items * Hq * 2;
+  const float* wo = ws + ws_o_offset(n_items, Hq);
   for (int k = 0; k < cnt; ++k) {
     const float* ml = ws + ((int64_t)(first + k) * Hq + h) * 2;
     const float sc = fast_exp2(ml[0] - M);

@@ -442,8 +442,7 @@ ds_status ds_blocked_attention_workspace_size(const ds_attn_params* params, int3
   if (max_seqs < 0 || max_tokens < 0 || max_blocks < 0 || !bytes)
     return fail(DS_ERR_INVALID_ARG, "negative capacity or NULL output");
   int64_t items = max_decode_items(max_seqs, max_blocks);
-  size_t per = (size_t)params->n_q_heads * (size_t)(params->head_dim + 2) * sizeof(float);
-  *bytes = align_up((size_t)items * per + 256, 256);
+  *bytes = align_up((size_t)dsr::ws_partial_bytes(items, params->n_q_heads, params->head_dim), 256);
   return DS_OK;
 }
 
@@ -457,8 +456,7 @@ ds_status ds_blocked_attention(const ds_ragged_meta* meta, const ds_attn_params*
   if (ds_status s = check_pool(pool, meta)) return s;
   if (!qkv || !aligned(qkv, 16)) return fail(DS_ERR_INVALID_ARG, "qkv NULL or not 16-byte aligned");
   if (!out || !aligned(out, 16)) return fail(DS_ERR_INVALID_ARG, "out NULL or not 16-byte aligned");
-  size_t need = (size_t)meta->n_decode_items * (size_t)params->n_q_heads *
-                    (size_t)(params->head_dim + 2) * sizeof(float);
+  const size_t need = (size_t)dsr::ws_partial_bytes(meta->n_decode_items, params->n_q_heads, params->head_dim);
   if (meta->n_decode_items > 0) {
     if (!workspace || !aligned(workspace, 256))
       return fail(DS_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
@@ -526,8 +524,8 @@ ds_status ds_fused_append_attention(const ds_ragged_meta* meta, const ds_attn_pa
   if (!qkv || !aligned(qkv, 16)) return fail(DS_ERR_INVALID_ARG, "qkv NULL or not 16-byte aligned");
   if (!out || !aligned(out, 16)) return fail(DS_ERR_INVALID_ARG, "out NULL or not 16-byte aligned");
   const size_t cb = fused_counter_bytes(params, meta->max_seqs);
-  const size_t need = cb + (size_t)meta->n_decode_items * (size_t)params->n_q_heads *
-                               (size_t)(params->head_dim + 2) * sizeof(float);
+  const size_t need = cb + (size_t)dsr::ws_partial_bytes(meta->n_decode_items, params->n_q_heads,
+                                                          params->head_dim);
   if (meta->n_decode_items > 0) {
     if (!workspace || !aligned(workspace, 256))
       return fail(DS_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");

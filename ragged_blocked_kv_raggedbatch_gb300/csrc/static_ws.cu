@@ -51,8 +51,7 @@ extern "C" ds_status ds_blocked_attention_static_ws(const ds_ragged_meta* meta,
   // Malformed arguments: let ds_blocked_attention report them.
   if (!meta || !params || params->n_q_heads <= 0 || params->head_dim <= 0 || meta->n_decode_items < 0)
     return ds_blocked_attention(meta, params, rope, qkv, pool, out, nullptr, 0, stream);
-  const size_t need = (size_t)meta->n_decode_items * (size_t)params->n_q_heads *
-                      (size_t)(params->head_dim + 2) * sizeof(float);
+  const size_t need = (size_t)dsr::ws_partial_bytes(meta->n_decode_items, params->n_q_heads, params->head_dim);
   if (need > kStaticBytes) {
     char msg[256];
     std::snprintf(msg, sizeof msg,

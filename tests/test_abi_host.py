@@ -310,7 +310,9 @@ def test_fused_call_validation_before_launch(lib):
         kw.get("ws_bytes", fused.value), None)
     assert call(out=None) == R.DS_ERR_INVALID_ARG
     assert call(qkv=FAKE_DEV + 2) == R.DS_ERR_INVALID_ARG
-    need = counters + pk.meta.n_decode_items * p.n_q_heads * (p.head_dim + 2) * 4
+    # partials: (m, l) pairs, then o from the next 256-byte boundary
+    items, hq = pk.meta.n_decode_items, p.n_q_heads
+    need = counters + (-(-items * hq * 2 // 64) * 64 + items * hq * p.head_dim) * 4
     assert pk.meta.n_decode_items > 0
     assert call(ws_bytes=need - 4) == R.DS_ERR_WORKSPACE
     assert call(ws=FAKE_DEV + 64) == R.DS_ERR_INVALID_ARG

@@ -54,6 +54,11 @@ EDGE = [
     ("gqa2_d128_fp16", [(700, 3), (50, 1), (0, 129)], 4, 2, 128, "fp16"),
     ("long_decode_many_splits", [(5000, 1), (3000, 1), (64 * 16 - 1, 1)], 8, 2, 128, "bf16"),
     ("g1_prefill_long", [(0, 300)], 2, 2, 128, "bf16"),
+    # odd query-head counts with an odd number of split items (3 + 2 and
+    # 3 + 8 splits of 4 blocks): the split partials' o region must stay
+    # 16-byte aligned whatever items * heads is
+    ("odd_heads3_split_decode", [(767, 1), (500, 1), (0, 40)], 3, 3, 64, "fp16"),
+    ("single_head_split_decode", [(767, 1), (2000, 1), (0, 5)], 1, 1, 128, "bf16"),
 ]
 
 

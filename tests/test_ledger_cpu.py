@@ -12,7 +12,8 @@ import oracle
 from ragged_blocked_kv_raggedbatch_gb300 import build as B
 from ragged_blocked_kv_raggedbatch_gb300 import ds_ragged as R
 from ragged_blocked_kv_raggedbatch_gb300 import workloads as W
-from ragged_blocked_kv_raggedbatch_gb300.splitfuse import NativeSplitFusePlanner, SplitFusePlanner
+from ragged_blocked_kv_raggedbatch_gb300.splitfuse import NativeSplitFusePlanner
+from splitfuse_model import SplitFusePlanner
 
 
 @pytest.fixture(scope="module", autouse=True)
