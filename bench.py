@@ -41,6 +41,9 @@ DEFAULT_WORKLOAD = "decode256_mha_d128"
 METRIC = "ragged attn new tokens/s per layer"
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# workloads whose oracle is also timed on one thread (the small and the
+# HBM-bound ones; the oracle's per-row cost is the same on any thread count)
+SINGLE_THREAD_ORACLE = ("tiny_gqa_d64", "decode256_mha_d128", "splitfuse2048_gqa_d128")
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
 # the dominant kernel from an ncu capture, keyed by workload; reported only
@@ -168,14 +171,62 @@ class ClockSampler:
 
 # ----------------------------------------------------------- CPU oracle legs
 
-def _oracle_sample(wl, n_rows_target: int, seed: int = 0, max_pool_bytes: float = 256e6):
-    """A bounded sample of the workload for the oracle: sequences drawn from
-    the batch; a prefill chunk contributes a random run of up to the remaining
-    row budget (as if it had been split there: seen += offset).  Returned as a
-    batch of its own over a compact pool (fresh values of the same
-    distribution, CPU generator), capped at ~max_pool_bytes of KV."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.split(":")[0].strip().lower() in ("model name", "cpu model"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def _spread_order(values: np.ndarray, seed: int) -> np.ndarray:
+    """Indices of `values` in an order whose every prefix spreads over their
+    range: sorted by value (ties shuffled), then visited at the positions of the
+    base-2 van der Corput sequence shifted by one half (the median first, then
+    the quartiles, ...), so that a short prefix already has about the mean of
+    the whole."""
+    n = len(values)
     rng = np.random.default_rng(seed)
-    order = rng.permutation(wl.n_seqs)
+    by_val = np.lexsort((rng.permutation(n), values))
+    bits = max(1, int(np.ceil(np.log2(max(n, 2)))) + 1)
+    seen, order = np.zeros(n, bool), []
+    for k in range(1 << bits):
+        r = (int("{:0{w}b}".format(k, w=bits)[::-1], 2) / float(1 << bits) + 0.5) % 1.0
+        i = min(n - 1, int(r * n))
+        if not seen[i]:
+            seen[i] = True
+            order.append(i)
+    order += [i for i in range(n) if not seen[i]]
+    return by_val[np.array(order, np.int64)]
+
+
+def _row_work(seen, new) -> float:
+    """Keys attended, summed over a batch's rows (the oracle's cost grows with it)."""
+    s = np.asarray(seen, np.float64)
+    n = np.asarray(new, np.float64)
+    return float((n * s + n * (n + 1) / 2).sum())
+
+
+def _oracle_sample(wl, n_rows_target: int, seed: int = 0, max_pool_bytes: float = 256e6):
+    """A bounded sample of the workload for the oracle: sequences taken in an
+    order spread over the batch's lengths (_spread_order); a prefill chunk
+    contributes a random run of up to the remaining row budget (as if it had
+    been split there: seen += offset).  Returned as a batch of its own over a
+    compact pool (fresh values of the same distribution, CPU generator), capped
+    at ~max_pool_bytes of KV."""
+    rng = np.random.default_rng(seed)
+    order = _spread_order(wl.seen.astype(np.int64) + wl.new, seed)
     block_bytes = 2 * wl.n_kv_heads * 64 * wl.head_dim * 2
     seqs, rows, blocks = [], 0, 0
     for i in order:
@@ -195,29 +246,50 @@ def _oracle_sample(wl, n_rows_target: int, seed: int = 0, max_pool_bytes: float 
                          name=wl.name + "_oracle_sample")
 
 
-def time_oracle(wl, seconds: float = 12.0, seed: int = 0):
-    """Tokens/s of the oracle on the host cores over a bounded sample, re-run
-    until about `seconds` of work.  Returns (tokens/s, threads, description, s)."""
+def _grow_sample(wl, seed: int, threads: int, pass_s: float):
+    """The smallest sample (_oracle_sample) whose one oracle pass takes about
+    pass_s seconds: start at a few rows and grow geometrically.  Returns
+    (sample, qkv, pool, seconds of its last pass)."""
     import oracle
-    threads = oracle.default_threads()
-    probe = _oracle_sample(wl, 1, seed + 1)
-    qkv, pool = W.make_values(probe, "cpu", seed=seed + 1)
-    t0 = time.perf_counter()
-    oracle.layer(probe, qkv, pool, n_threads=threads)
-    per_row = max(time.perf_counter() - t0, 1e-5) / probe.n_tokens
-    sub = _oracle_sample(wl, int(max(1, min(wl.n_tokens, seconds / per_row))), seed)
-    qkv, pool = W.make_values(sub, "cpu", seed=seed)
-    rows, t0 = 0, time.perf_counter()
+    rows, last_n = 4, -1
+    while True:
+        sub = _oracle_sample(wl, rows, seed)
+        qkv, pool = W.make_values(sub, "cpu", seed=seed)
+        t0 = time.perf_counter()
+        oracle.layer(sub, qkv, pool, n_threads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= pass_s or sub.n_tokens >= wl.n_tokens or sub.n_tokens == last_n:
+            return sub, qkv, pool, dt
+        last_n = sub.n_tokens
+        rows = min(wl.n_tokens, int(rows * min(8.0, max(2.0, 0.8 * pass_s / max(dt, 1e-4)))))
+
+
+def time_oracle(wl, seconds: float = 10.0, seed: int = 0, threads: int = 0):
+    """The oracle (metadata, append, attention in fp64) on the host cores over a
+    bounded sample of the workload, re-run until about `seconds` of work, and
+    scaled to the whole batch by the keys its rows attend: tokens/s of the
+    batch = N / (sample time x batch work / sample work).  Returns a dict."""
+    import oracle
+    threads = threads or oracle.default_threads()
+    sub, qkv, pool, _ = _grow_sample(wl, seed, threads, seconds / 4)
+    reps, t0 = 0, time.perf_counter()
     while True:
         oracle.layer(sub, qkv, pool, n_threads=threads)
-        rows += sub.n_tokens
+        reps += 1
         dt = time.perf_counter() - t0
         if dt >= seconds:
             break
-    desc = ("%d rows (%d sequences, %d KV-history tokens) sampled from %s, fresh values of the "
-            "same distribution, fp64 oracle meta+append+attention, repeated to %.1f s" %
-            (sub.n_tokens, sub.n_seqs, int(sub.seen.sum()), wl.name, dt))
-    return rows / dt, threads, desc, dt
+    batch_work = _row_work(wl.seen, wl.new)
+    sub_work = _row_work(sub.seen, sub.new)
+    batch_s = dt / reps * batch_work / sub_work
+    return {"value": wl.n_tokens / batch_s, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "seconds": dt, "batch_seconds_est": batch_s,
+            "sample": ("%d rows (%d sequences, %d KV-history tokens, mean history %.0f vs the batch's %.0f) "
+                       "sampled from %s in length-spread order, fresh values of the same distribution; "
+                       "fp64 oracle metadata+append+attention repeated %d times (%.1f s); scaled to the "
+                       "whole batch by keys attended (batch/sample = %.1f)"
+                       % (sub.n_tokens, sub.n_seqs, int(sub.seen.sum()), float(sub.seen.mean()),
+                          float(wl.seen.mean()), wl.name, reps, dt, batch_work / sub_work))}
 
 
 def _l2_note(wl) -> str:
@@ -244,36 +316,35 @@ def reference_arm(args, wl):
     # size each step so that warmup + steps take about two minutes
     budget_s = 120.0
     steps = args.steps + args.warmup
-    probe = _oracle_sample(wl, 1, 99)
-    qkv, pool = W.make_values(probe, "cpu", seed=99)
-    t0 = time.perf_counter()
-    oracle.layer(probe, qkv, pool, n_threads=threads)
-    per_row = max(time.perf_counter() - t0, 1e-5) / probe.n_tokens
-    rows = int(max(1, min(wl.n_tokens, budget_s / steps / per_row)))
+    first = _grow_sample(wl, 0, threads, budget_s / steps)[0]
+    rows = first.n_tokens
+    batch_work = _row_work(wl.seen, wl.new)
     samples = []
     for k in range(min(steps, 4)):
         sub = _oracle_sample(wl, rows, k)
         samples.append((sub,) + tuple(W.make_values(sub, "cpu", seed=k)))
-    times, toks = [], 0
+    batch_s = []
     for k in range(steps):
         sub, qkv, pool = samples[k % len(samples)]
         t0 = time.perf_counter()
         oracle.layer(sub, qkv, pool, n_threads=threads)
         dt = time.perf_counter() - t0
         if k >= args.warmup:
-            times.append(dt)
-            toks += sub.n_tokens
-    total = float(sum(times))
-    value = toks / total
+            # this step's sample time, scaled to the whole batch by keys attended
+            batch_s.append(dt * batch_work / _row_work(sub.seen, sub.new))
+    total = float(sum(batch_s))
+    value = wl.n_tokens * len(batch_s) / total
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * total / max(1, len(times)), "higher_is_better": True,
+        "ms_per_step": 1e3 * total / max(1, len(batch_s)), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": run_config(wl, args, ws),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": "about %d rows per step (%d in the first sample) drawn from %s "
-                                   "(fresh values, same distribution; 4 samples reused)"
+                         "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+                         "sample": "about %d rows per step (%d in the first sample) drawn from %s in "
+                                   "length-spread order (fresh values, same distribution; 4 samples "
+                                   "reused); each step's time scaled to the whole batch by keys attended"
                                    % (rows, samples[0][0].n_tokens, wl.name)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -283,18 +354,39 @@ def reference_arm(args, wl):
 
 # ----------------------------------------------------------------- GPU arm
 
-def gpu_arm(args, wl):
+def _roofline(r_bytes, r_flops, mean_s, peaks, sustained=False):
+    """The roofline object of a launch group: the slower of its bytes over the
+    HBM peak and its flops over the bf16 tensor peak decides the bound."""
+    tf_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    if r_bytes / (peaks["hbm_gbs"] * 1e9) >= r_flops / (tf_peak * 1e12):
+        achieved = r_bytes / mean_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "frac_vs_8tbs": achieved / 8000.0}
+        if roof["frac"] > 1.0:
+            roof["note"] = ("achieved above the measured copy peak: that peak is a read+write copy, "
+                            "this launch group mostly reads")
+    else:
+        achieved = r_flops / mean_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": achieved / tf_peak}
+        if not sustained:
+            roof["frac_of_sustained"] = achieved / peaks["bf16_tflops_sustained"]
+    return roof
+
+
+def device_measure(wl, args, grp, local, K, warmup, keep=False, flushed_loop=True):
+    """K timed steps of one workload, inputs resident in HBM, CUDA events on
+    the launching stream around each step and around its attention call; the
+    SM clocks sampled meanwhile.  Returns a dict (and, with keep, the live
+    objects the end-to-end leg reuses)."""
     import torch
     from ragged_blocked_kv_raggedbatch_gb300 import ds_ragged as R
 
-    ws, rank, local = replicas.env()
-    torch.cuda.set_device(local)
-    grp = replicas.Group("nccl")
+    ws, rank, _ = replicas.env()
     dev = "cuda"
     stream = torch.cuda.Stream()
-    peaks = load_peaks()
-    alg = algorithmic(wl)
     nb_total = int(wl.blocks_needed().sum())
+    alg = algorithmic(wl)
     with torch.cuda.stream(stream):
         qkv, pool = W.make_values(wl, dev, seed=replicas.rank_seed(wl.seed, rank))
         params = R.params_for(wl)
@@ -318,27 +410,29 @@ def gpu_arm(args, wl):
         launches_per_step = 1 + (m.n_prefill_tiles > 0) + (m.n_decode_items > 0) + \
             (m.n_decode_items > m.n_decode_seqs)
 
-    def step():
+    def run_step(b_event=None):
         if fused:
+            if b_event is not None:
+                b_event.record(stream)
             layer.fused(qkv, pool, out)
         else:
             layer.append(qkv, pool)
+            if b_event is not None:
+                b_event.record(stream)
             layer.attention(qkv, pool, out)
 
     flush = None
-    step_bytes = alg["bytes"]
-    if step_bytes < 2 * L2_BYTES:
+    if alg["bytes"] < 2 * L2_BYTES:
         flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
-
-    for _ in range(args.warmup):
-        step()
-        if flush is not None:
-            flush.zero_()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            run_step()
+            if flush is not None:
+                flush.zero_()
     stream.synchronize()
     grp.barrier()
     torch.cuda.synchronize()
 
-    K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     with ClockSampler(local) as clk:
@@ -346,13 +440,7 @@ def gpu_arm(args, wl):
             for k in range(K):
                 a, b, c = ev[k]
                 a.record(stream)
-                if fused:
-                    b.record(stream)
-                    layer.fused(qkv, pool, out)
-                else:
-                    layer.append(qkv, pool)
-                    b.record(stream)
-                    layer.attention(qkv, pool, out)
+                run_step(b)
                 c.record(stream)
                 if flush is not None:
                     flush.zero_()
@@ -362,7 +450,7 @@ def gpu_arm(args, wl):
     # next to the main loop's (which flushes only when a step's bytes are
     # below twice L2)
     flushed = None
-    if flush is None:
+    if flush is None and flushed_loop:
         fl = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
         K2 = max(3, min(K, 50))
         ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
@@ -372,13 +460,7 @@ def gpu_arm(args, wl):
                 fl.zero_()
                 a, b, c = ev2[k]
                 a.record(stream)
-                if fused:
-                    b.record(stream)
-                    layer.fused(qkv, pool, out)
-                else:
-                    layer.append(qkv, pool)
-                    b.record(stream)
-                    layer.attention(qkv, pool, out)
+                run_step(b)
                 c.record(stream)
         stream.synchronize()
         flushed = {"ms_per_step": float(np.mean([a.elapsed_time(c) for a, b, c in ev2])),
@@ -389,24 +471,16 @@ def gpu_arm(args, wl):
     app_ms = [a.elapsed_time(b) for a, b, c in ev]
     total_ms = grp.max(float(sum(step_ms)), dev)
     torch.cuda.synchronize()
+    peaks = load_peaks()
     ms_per_step = total_ms / K
-    value = ws * wl.n_tokens * K / (total_ms / 1e3)
-
     # roofline of the attention call (the dominant launches); the fused call
-    # also does the append, so it is held to the whole step's work
+    # also does the append, so it is held to the whole step's work.  A loop
+    # of a second or more runs at the sustained tensor clock.
     attn_mean_s = float(np.mean(attn_ms)) / 1e3
     r_bytes = alg["bytes"] if fused else alg["attn_bytes"]
     r_flops = alg["flops"] if fused else alg["attn_flops"]
-    hbm_t = r_bytes / (peaks["hbm_gbs"] * 1e9)
-    tc_t = r_flops / (peaks["bf16_tflops"] * 1e12)
-    if hbm_t >= tc_t:
-        achieved = r_bytes / attn_mean_s / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"]}
-    else:
-        achieved = r_flops / attn_mean_s / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"]}
+    long_loop = total_ms >= 1000.0
+    roof = _roofline(r_bytes, r_flops, attn_mean_s, peaks, sustained=long_loop)
     rec = NCU_TRAFFIC.get(wl.name + (":fused" if fused else ""))
     roof["traffic"] = rec["bytes"] if rec and rec.get("src") == _src_hash(rec["files"]) else None
     parts = ("decode split-K + combine" if m.n_prefill_tiles == 0 else
@@ -417,102 +491,185 @@ def gpu_arm(args, wl):
     roof["algorithmic_bytes"] = r_bytes
     roof["algorithmic_flops"] = r_flops
     roof["mean_ms"] = attn_mean_s * 1e3
+    # whole-step roofline: T_roof = max(bytes / HBM peak, flops / tensor peak)
+    tf = peaks["bf16_tflops_sustained" if long_loop else "bf16_tflops"]
+    t_roof = max(alg["bytes"] / (peaks["hbm_gbs"] * 1e9), alg["flops"] / (tf * 1e12))
+    res = {
+        "value": ws * wl.n_tokens * K / (total_ms / 1e3), "ms_per_step": ms_per_step, "steps": K,
+        "roofline": roof, "step_roofline_frac": t_roof / (ms_per_step / 1e3),
+        "t_roof_ms": t_roof * 1e3, "clocks": clocks,
+        "append_ms": float(np.mean(app_ms)), "attention_ms": float(np.mean(attn_ms)),
+        "decode_kv_gbps": alg["kv_history_bytes"] / attn_mean_s / 1e9,
+        "algorithmic": {"flops": alg["flops"], "bytes": alg["bytes"]},
+        "meta_build_us": meta_build_us, "l2_flushed": flushed, "l2": _l2_note(wl),
+        "launches_per_step": int(launches_per_step),
+        "workspace_bytes": int(m.n_decode_items * wl.n_q_heads * (wl.head_dim + 2) * 4),
+        # bytes the implementation moves: the append (K, V read and written),
+        # the attention call (Q, every KV row incl. the new ones, O, block ids)
+        # and the split-K partials (written, then read by the merge)
+        "implemented_bytes": int(alg["append_bytes"] + alg["attn_bytes"] +
+                                 2 * m.n_decode_items * wl.n_q_heads * (wl.head_dim + 2) * 4),
+    }
+    if keep:
+        res["_live"] = dict(stream=stream, qkv=qkv, pool=pool, out=out, layer=layer, params=params,
+                            descs=descs, nb_total=nb_total, fused=fused)
+    else:
+        del qkv, pool, out, layer, flush
+        torch.cuda.empty_cache()
+    return res
 
-    # whole-step roofline (slower of bytes/BW and flops/peak) as a fraction
-    t_roof = max(alg["bytes"] / (peaks["hbm_gbs"] * 1e9), alg["flops"] / (peaks["bf16_tflops"] * 1e12))
-    step_frac = t_roof / (ms_per_step / 1e3)
 
-    # ---- end to end through the C ABI from pinned host buffers.  Every step
-    # copies its qkv rows in from pinned host memory, uploads its metadata,
-    # runs the layer and copies its output rows back to pinned host memory.
-    # Steps are pipelined the way a serving loop would run them: copy-in,
-    # compute and copy-out on three streams over two device buffer sets (and
-    # two metadata objects, so a pinned staging buffer is never rewritten while
-    # its upload may still be pending), ordered by events.
-    e2e = None
-    if not args.no_e2e:
+def e2e_measure(wl, args, grp, live, K):
+    """The metric end to end through the C ABI: every step copies its qkv rows
+    in from pinned host memory, uploads its metadata, runs the layer and copies
+    its output rows back to pinned host memory.  Steps are pipelined the way a
+    serving loop would run them: copy-in, compute and copy-out on three streams
+    over two device buffer sets (and two metadata objects, so a pinned staging
+    buffer is never rewritten while its upload may still be pending), ordered
+    by events."""
+    import torch
+    from ragged_blocked_kv_raggedbatch_gb300 import ds_ragged as R
+
+    ws, _, _ = replicas.env()
+    dev = "cuda"
+    stream, qkv, pool, out = live["stream"], live["qkv"], live["pool"], live["out"]
+    layer, params, descs, fused = live["layer"], live["params"], live["descs"], live["fused"]
+    with torch.cuda.stream(stream):
+        qkv_host = qkv.cpu().pin_memory()
+        out_host = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+        qkv_d = [qkv, torch.empty_like(qkv)]
+        out_d = [out, torch.empty_like(out)]
+        layers = [layer, R.RaggedLayer(params, wl.n_seqs, wl.n_tokens, live["nb_total"], wl.max_len(),
+                                       stream=stream)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    ev_meta = [None, None]
+
+    def issue(k):
+        b = k % 2
+        with torch.cuda.stream(s_in):
+            if k >= 2:
+                s_in.wait_event(ev_done[b])  # step k-2 no longer reads qkv_d[b]
+            qkv_d[b].copy_(qkv_host, non_blocking=True)
+            ev_in[b].record(s_in)
+        if ev_meta[b] is not None:
+            ev_meta[b].synchronize()  # step k-2's metadata upload left the staging buffer
         with torch.cuda.stream(stream):
-            qkv_host = qkv.cpu().pin_memory()
-            out_host = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-            qkv_d = [qkv, torch.empty_like(qkv)]
-            out_d = [out, torch.empty_like(out)]
-            layers = [layer, R.RaggedLayer(params, wl.n_seqs, wl.n_tokens, nb_total, wl.max_len(), stream=stream)]
-        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_done = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
-        ev_meta = [None, None]
+            stream.wait_event(ev_in[b])
+            if k >= 2:
+                stream.wait_event(ev_out[b])  # step k-2's output is on the host
+            layers[b].build(descs, wl.num_blocks)
+            ev_meta[b] = torch.cuda.Event()
+            ev_meta[b].record(stream)
+            if fused:
+                layers[b].fused(qkv_d[b], pool, out_d[b])
+            else:
+                layers[b].append(qkv_d[b], pool)
+                layers[b].attention(qkv_d[b], pool, out_d[b])
+            ev_done[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[b])
+            out_host[b].copy_(out_d[b], non_blocking=True)
+            ev_out[b].record(s_out)
 
-        def issue(k):
-            b = k % 2
-            with torch.cuda.stream(s_in):
-                if k >= 2:
-                    s_in.wait_event(ev_done[b])  # step k-2 no longer reads qkv_d[b]
-                qkv_d[b].copy_(qkv_host, non_blocking=True)
-                ev_in[b].record(s_in)
-            if ev_meta[b] is not None:
-                ev_meta[b].synchronize()  # step k-2's metadata upload left the staging buffer
-            with torch.cuda.stream(stream):
-                stream.wait_event(ev_in[b])
-                if k >= 2:
-                    stream.wait_event(ev_out[b])  # step k-2's output is on the host
-                layers[b].build(descs, wl.num_blocks)
-                ev_meta[b] = torch.cuda.Event()
-                ev_meta[b].record(stream)
-                if fused:
-                    layers[b].fused(qkv_d[b], pool, out_d[b])
-                else:
-                    layers[b].append(qkv_d[b], pool)
-                    layers[b].attention(qkv_d[b], pool, out_d[b])
-                ev_done[b].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_done[b])
-                out_host[b].copy_(out_d[b], non_blocking=True)
-                ev_out[b].record(s_out)
+    E = max(3, min(K, 200))
+    for k in range(4):  # warm-up of the pipeline (both buffer sets)
+        issue(k)
+    torch.cuda.synchronize()
+    grp.barrier()
+    t0 = time.perf_counter()
+    for k in range(E):
+        issue(k)
+    torch.cuda.synchronize()  # every step's output is on the host
+    e2e_s = grp.max(time.perf_counter() - t0, dev)
+    return {"value": ws * wl.n_tokens * E / e2e_s, "unit": "tokens/s",
+            "h2d_bytes_per_step": int(qkv.numel() * qkv.element_size() + layer.meta.used_bytes),
+            "d2h_bytes_per_step": int(out.numel() * out.element_size()), "steps": E,
+            "pipelined": "copy-in / compute / copy-out streams, 2 buffer sets"}
 
-        E = max(3, min(K, 200))
-        for k in range(4):  # warm-up of the pipeline (both buffer sets)
-            issue(k)
-        torch.cuda.synchronize()
-        grp.barrier()
-        t0 = time.perf_counter()
-        for k in range(E):
-            issue(k)
-        torch.cuda.synchronize()  # every step's output is on the host
-        e2e_s = grp.max(time.perf_counter() - t0, dev)
-        e2e = {"value": ws * wl.n_tokens * E / e2e_s, "unit": "tokens/s",
-               "h2d_bytes_per_step": int(qkv.numel() * qkv.element_size() + m.used_bytes),
-               "d2h_bytes_per_step": int(out.numel() * out.element_size()), "steps": E,
-               "pipelined": "copy-in / compute / copy-out streams, 2 buffer sets"}
+
+def _per_workload_entry(wl, r) -> dict:
+    keep = ("value", "ms_per_step", "steps", "step_roofline_frac", "t_roof_ms", "clocks",
+            "attention_ms", "append_ms", "launches_per_step", "l2", "l2_flushed")
+    d = {k: r[k] for k in keep}
+    d["unit"] = "tokens/s"
+    d["roofline"] = {k: r["roofline"][k] for k in ("bound", "achieved", "peak", "unit", "frac")
+                     if k in r["roofline"]}
+    for k in ("frac_of_sustained", "frac_vs_8tbs"):
+        if k in r["roofline"]:
+            d["roofline"][k] = r["roofline"][k]
+    d["dtype"] = wl.dtype
+    d["seed"] = wl.seed
+    return d
+
+
+def gpu_arm(args, wl):
+    import torch
+
+    ws, rank, local = replicas.env()
+    torch.cuda.set_device(local)
+    grp = replicas.Group("nccl")
+    K = args.steps
+    head = device_measure(wl, args, grp, local, K, args.warmup, keep=True)
+    e2e = None if args.no_e2e else e2e_measure(wl, args, grp, head["_live"], K)
+    del head["_live"]
+    torch.cuda.empty_cache()
+
+    # every named workload (seed 0) on the same clock, as the headline's
+    # neighbours: the headline workload's own entry is its measurement above
+    per_workload = None
+    if not args.no_per_workload:
+        per_workload = {}
+        for name in sorted(W.WORKLOADS):
+            if name == wl.name and wl.seed == 0:
+                per_workload[name] = _per_workload_entry(wl, head)
+                continue
+            w2 = W.make_workload(name, 0)
+            per_workload[name] = _per_workload_entry(
+                w2, device_measure(w2, args, grp, local, K, args.warmup, flushed_loop=False))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        v, cores, desc, dt = time_oracle(wl, seconds=args.cpu_seconds)
-        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
-               "seconds": dt}
+        cpu = time_oracle(wl, seconds=args.cpu_seconds)
+        cpu["cpu_model"] = cpu_model()
+        cpu["nproc"] = os.cpu_count()
+        # the oracle on every workload: all cores, and one thread where a
+        # single thread finishes a sample in seconds
+        if per_workload is not None:
+            per = {}
+            for name in sorted(W.WORKLOADS):
+                w2 = wl if (name == wl.name and wl.seed == 0) else W.make_workload(name, 0)
+                allc = cpu if w2 is wl else time_oracle(w2, seconds=args.cpu_seconds / 3)
+                entry = {"all_cores": {"value": allc["value"], "cores": allc["cores"],
+                                       "batch_seconds_est": allc["batch_seconds_est"]}}
+                if name in SINGLE_THREAD_ORACLE:
+                    one = time_oracle(w2, seconds=args.cpu_seconds / 3, threads=1)
+                    entry["single_thread"] = {"value": one["value"], "cores": 1,
+                                              "batch_seconds_est": one["batch_seconds_est"]}
+                per[name] = entry
+            cpu["per_workload"] = per
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
             "config": run_config(wl, args, ws),
-            "roofline": roof,
-            "step_roofline_frac": step_frac,
-            "decode_kv_gbps": alg["kv_history_bytes"] / (float(np.mean(attn_ms)) / 1e3) / 1e9,
-            "append_ms": float(np.mean(app_ms)), "attention_ms": float(np.mean(attn_ms)),
-            "algorithmic": {"flops": alg["flops"], "bytes": alg["bytes"]},
-            "hbm_frac_vs_8tbs": (alg["attn_bytes"] / attn_mean_s / 1e9) / 8000.0,
-            "meta_build_us": meta_build_us,
-            "l2_flushed": flushed,
-            # bytes the implementation moves: the append (K, V read and written),
-            # the attention call (Q, every KV row incl. the new ones, O, block
-            # ids) and the split-K partials (written, then read by the merge)
-            "workspace_bytes": int(m.n_decode_items * wl.n_q_heads * (wl.head_dim + 2) * 4),
-            "implemented_bytes": int(alg["append_bytes"] + alg["attn_bytes"] +
-                                     2 * m.n_decode_items * wl.n_q_heads * (wl.head_dim + 2) * 4),
-            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches_per_step * K,
-            "clocks": clocks,
+            "roofline": head["roofline"],
+            "step_roofline_frac": head["step_roofline_frac"],
+            "decode_kv_gbps": head["decode_kv_gbps"],
+            "append_ms": head["append_ms"], "attention_ms": head["attention_ms"],
+            "algorithmic": head["algorithmic"],
+            "hbm_frac_vs_8tbs": head["roofline"].get("frac_vs_8tbs"),
+            "meta_build_us": head["meta_build_us"],
+            "l2_flushed": head["l2_flushed"],
+            "workspace_bytes": head["workspace_bytes"],
+            "implemented_bytes": head["implemented_bytes"],
+            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": head["launches_per_step"] * K,
+            "clocks": head["clocks"],
+            "per_workload": per_workload,
         }
         print(json.dumps(line), flush=True)
     grp.close()
@@ -754,7 +911,10 @@ def main(argv=None):
                          "fused: ds_fused_append_attention")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="oracle time of the headline workload's CPU baseline (the others take a third)")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="time only the chosen workload (no per_workload object)")
     ap.add_argument("--component", choices=["offload", "gather", "multistep", "graph"], default=None,
                     help="measure a component next to the layer instead of the layer step")
     args = ap.parse_args(argv)

@@ -63,3 +63,21 @@ def test_source_hash_ignores_comments_and_blank_space(tmp_path, monkeypatch):
     assert bench._src_hash(["k.cu"]) == h0
     (csrc / "k.cu").write_text("int f(int x) {\n  return x + 2;\n}\n")
     assert bench._src_hash(["k.cu"]) != h0
+
+
+def test_spread_order_is_a_permutation_whose_prefixes_track_the_mean():
+    vals = W.make_workload("decode256_mha_d128").seen.astype(np.int64)
+    order = bench._spread_order(vals, 0)
+    assert sorted(order.tolist()) == list(range(len(vals)))
+    # the median first; every prefix of 8 or more within 10% of the batch mean
+    assert vals[order[0]] == np.sort(vals)[len(vals) // 2]
+    for k in (8, 16, 32, 64):
+        assert abs(vals[order[:k]].mean() - vals.mean()) <= 0.1 * vals.mean(), k
+    odd = np.array([5, 1, 9, 3, 7], np.int64)
+    assert sorted(bench._spread_order(odd, 1).tolist()) == list(range(5))
+
+
+def test_row_work_counts_keys_attended():
+    seen, new = [0, 90, 130, 7], [37, 1, 64, 1]
+    brute = sum(s + j + 1 for s, n in zip(seen, new) for j in range(n))
+    assert bench._row_work(seen, new) == brute
