@@ -192,21 +192,27 @@ def cpu_model() -> str:
 
 def _spread_order(values: np.ndarray, seed: int) -> np.ndarray:
     """Indices of `values` in an order whose every prefix spreads over their
-    range: sorted by value (ties shuffled), then visited at the positions of the
-    base-2 van der Corput sequence shifted by one half (the median first, then
-    the quartiles, ...), so that a short prefix already has about the mean of
-    the whole."""
+    range: sorted by value (ties shuffled), then visited at quantile midpoints
+    level by level -- 1/2; 1/4, 3/4; 3/8, 5/8, 1/8, 7/8; ... -- each level's
+    points taken inside-out in symmetric pairs, so that a short prefix already
+    has about the mean of the whole."""
     n = len(values)
     rng = np.random.default_rng(seed)
     by_val = np.lexsort((rng.permutation(n), values))
-    bits = max(1, int(np.ceil(np.log2(max(n, 2)))) + 1)
     seen, order = np.zeros(n, bool), []
-    for k in range(1 << bits):
-        r = (int("{:0{w}b}".format(k, w=bits)[::-1], 2) / float(1 << bits) + 0.5) % 1.0
-        i = min(n - 1, int(r * n))
-        if not seen[i]:
-            seen[i] = True
-            order.append(i)
+    levels = int(np.ceil(np.log2(max(n, 2)))) + 2
+    for m in range(1, levels + 1):
+        half = 1 << (m - 1)
+        pts = []
+        for j in reversed(range((half + 1) // 2)):
+            pts.append((2 * j + 1) / float(1 << m))
+            if half - 1 - j != j:
+                pts.append((2 * (half - 1 - j) + 1) / float(1 << m))
+        for r in pts:
+            i = min(n - 1, int(r * n))
+            if not seen[i]:
+                seen[i] = True
+                order.append(i)
     order += [i for i in range(n) if not seen[i]]
     return by_val[np.array(order, np.int64)]
 
