@@ -19,6 +19,8 @@ enum : int {
   HDR_S = 1,
   HDR_N = 2,
   HDR_BLOCKS = 3,
+  HDR_DEC_NEXT = 4,  // decode units handed out so far (tensor-core decode kernel)
+  HDR_DEC_DONE = 5,  // its CTAs that finished; the last one zeroes both words
   HDR_WORDS = 16,
 };
 
@@ -169,6 +171,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of phase `parity` (try_wait may suspend the thread for a
+// while; a loop that polls several barriers must not).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of an mbarrier, giving up after ~`limit_cycles` SM
 // cycles.  Returns false on timeout (the caller records an error and stops
 // issuing work; it never spins forever).
@@ -225,6 +240,14 @@ cudaError_t launch_decode(const ds_ragged_meta& m, const LayerArgs& a, const voi
                           const void* pool, void* out, float* ws, cudaStream_t st,
                           bool overlap_previous, bool fused_append = false,
                           int32_t* counters = nullptr);
+// Decode rows of grouped-query layers (G >= 2, D = 128) on the tensor cores;
+// the same arguments and results as launch_decode (decode_tc.cu).
+cudaError_t launch_decode_tc(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
+                             const void* pool, void* out, float* ws, cudaStream_t st,
+                             bool overlap_previous, bool fused_append, int32_t* counters);
+// The merge of the split partials of multi-split decode rows (decode.cu).
+cudaError_t launch_decode_combine(const ds_ragged_meta& m, const LayerArgs& a, const float* ws,
+                                  void* out, cudaStream_t st);
 cudaError_t launch_prefill(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
                            const void* pool, void* out, cudaStream_t st);
 

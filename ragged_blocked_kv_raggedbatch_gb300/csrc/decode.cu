@@ -61,6 +61,11 @@
 #ifndef DSR_DECODE_LAZY
 #define DSR_DECODE_LAZY 1
 #endif
+// 1: decode rows of grouped-query layers with head size 128 run on the
+// tensor-core kernel (decode_tc.cu); 0: every decode row runs here.
+#ifndef DSR_DECODE_TC
+#define DSR_DECODE_TC 1
+#endif
 
 namespace dsr {
 
@@ -562,14 +567,23 @@ static cudaError_t launch_decode_t(const ds_ragged_meta& m, const LayerArgs& a, 
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (counters == nullptr && m.n_decode_items > m.n_decode_seqs) {
-    dim3 g2(m.n_decode_seqs, (a.Hq + 3) / 4);
-    decode_combine_kernel<BF16, D><<<g2, 128, 0, st>>>(
-        reinterpret_cast<const int4*>(m.decode_seqs), ws, static_cast<uint16_t*>(out),
-        m.n_decode_items, a.Hq);
-    e = cudaGetLastError();
-  }
+  if (counters == nullptr && m.n_decode_items > m.n_decode_seqs) e = launch_decode_combine(m, a, ws, out, st);
   return e;
+}
+
+cudaError_t launch_decode_combine(const ds_ragged_meta& m, const LayerArgs& a, const float* ws,
+                                  void* out, cudaStream_t st) {
+  dim3 g2(m.n_decode_seqs, (a.Hq + 3) / 4);
+  const int4* dseqs = reinterpret_cast<const int4*>(m.decode_seqs);
+  uint16_t* o = static_cast<uint16_t*>(out);
+  if (a.dtype == DS_BF16) {
+    if (a.D == 128) decode_combine_kernel<true, 128><<<g2, 128, 0, st>>>(dseqs, ws, o, m.n_decode_items, a.Hq);
+    else decode_combine_kernel<true, 64><<<g2, 128, 0, st>>>(dseqs, ws, o, m.n_decode_items, a.Hq);
+  } else {
+    if (a.D == 128) decode_combine_kernel<false, 128><<<g2, 128, 0, st>>>(dseqs, ws, o, m.n_decode_items, a.Hq);
+    else decode_combine_kernel<false, 64><<<g2, 128, 0, st>>>(dseqs, ws, o, m.n_decode_items, a.Hq);
+  }
+  return cudaGetLastError();
 }
 
 template <bool BF16, bool HALF, int D>
@@ -596,6 +610,11 @@ static cudaError_t launch_decode_d(const ds_ragged_meta& m, const LayerArgs& a, 
 cudaError_t launch_decode(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
                           const void* pool, void* out, float* ws, cudaStream_t st,
                           bool overlap_previous, bool fused_append, int32_t* counters) {
+#if DSR_DECODE_TC
+  // grouped-query rows of head size 128: the tensor-core kernel (decode_tc.cu)
+  if (a.D == 128 && a.G >= 2)
+    return launch_decode_tc(m, a, qkv, pool, out, ws, st, overlap_previous, fused_append, counters);
+#endif
   const bool half = a.style == DS_ROPE_HALF;
   const bool ov = overlap_previous, fu = fused_append;
   if (a.dtype == DS_BF16)

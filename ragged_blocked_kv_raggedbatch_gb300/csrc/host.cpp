@@ -16,8 +16,14 @@
 
 #include "common.cuh"
 
-#ifndef DSR_PREFILL_SM_FACTOR
-#define DSR_PREFILL_SM_FACTOR 2.2
+// Decode-rate constants of the prefill/decode SM split (GB/s, GB300): the HBM
+// rate of the decode rows and the rate one SM of the tensor-core decode kernel
+// reaches.
+#ifndef DSR_DEC_GBPS
+#define DSR_DEC_GBPS 6700.0
+#endif
+#ifndef DSR_DEC_SM_GBPS
+#define DSR_DEC_SM_GBPS 90.0
 #endif
 
 namespace {
@@ -64,6 +70,10 @@ ds_status check_params(const ds_attn_params* p) {
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// SMs of the GPU the host-side cost models assume (GB300); the launches clamp
+// to the device's real count.
+constexpr int kModelSMs = 152;
 
 // Upper bounds of the work lists for given capacities.
 int64_t max_prefill_tiles(int64_t max_seqs, int64_t max_tokens) { return max_seqs + max_tokens; }
@@ -252,7 +262,7 @@ ds_status ds_ragged_meta_pack(const ds_seq_desc* seqs, int32_t n_seqs,
   // 1.341 ms, 16: 1.299, 32: 1.289).
   int split = dsr::kMaxSplitBlocks;
   while (split > dsr::kMinSplitBlocks &&
-         dec_blocks * params->n_kv_heads < (int64_t)8 * 3 * 152 * split)
+         dec_blocks * params->n_kv_heads < (int64_t)8 * 3 * kModelSMs * split)
     split >>= 1;
   int64_t n_items = 0;
   for (int32_t i = 0; i < n_seqs; ++i) {
@@ -347,24 +357,49 @@ ds_status ds_ragged_meta_pack(const ds_seq_desc* seqs, int32_t n_seqs,
   m->max_len = (int32_t)max_len;
   m->pool_num_blocks = pool_num_blocks;
   m->split_blocks = split;
-  // SMs for the persistent prefill grid when decode rows run beside it: enough
-  // for the prefill atoms to finish well within the time the decode rows take
-  // to stream their KV history.  Costs measured on GB300 with the first
-  // persistent kernel: ~1.8 us per 128-key step of a two-tile atom (1.2 us
-  // with one tile); decode KV at ~6.4 TB/s.  The margin (DSR_PREFILL_SM_FACTOR)
-  // was swept on GB300: SplitFuse 2048 at 1.0 / 1.25 / 1.6 / 2.2: 2.08 / 1.79 /
-  // 1.59 / 1.35 ms.  With the faster prefill kernel (~1.4 us per two-tile step)
-  // the share matters little above 1.6: SplitFuse 1.6 / 2.2 / 3.0 / all SMs
-  // 1.357 / 1.357 / 1.354 / 1.349 ms, max ragged within 1.5 % from 1.2 to all
-  // SMs (its decode CTAs take as long on few SMs as on many).
+  // SMs for the persistent prefill grid when decode rows run beside it.  The
+  // prefill atoms cost T_PRE (SM-us) in all: ~1.8 us per 128-key step of a
+  // two-tile atom, ~1.2 us with one tile (GB300; the sum matches the measured
+  // prefill-only time of the max ragged batch within 4%).  The decode rows
+  // stream their KV history at up to DSR_DEC_SM_GBPS per SM and DSR_DEC_GBPS
+  // in all; decode CTAs take the SMs the prefill grid leaves, and every SM once
+  // prefill is done.  The grid is the P minimising the finish time
+  //   T(P) = T_PRE / P                        if decode is done by then,
+  //          T_PRE / P + (rest of the KV) / rate(all SMs)   otherwise,
+  // over P in [1, kModelSMs - 1].  (A fixed share, as an earlier kernel used,
+  // let the prefill grid take 143 of 152 SMs on the max ragged batch and left
+  // the decode rows to run after it.)
   m->prefill_sms = 0.f;
   if (!tv.empty() && dec_blocks > 0) {
     double pre_us = 0.0;
     for (const Tile& t : tv)
       pre_us += (double)((t.kv_len + 127) / 128) * (t.ntok > tile_tokens / 2 ? 1.8 : 1.2);
     pre_us *= params->n_kv_heads;
-    const double dec_us = (double)dec_blocks * params->n_kv_heads * 2.0 * bs * params->head_dim * 2.0 / 6.4e6;
-    m->prefill_sms = (float)(DSR_PREFILL_SM_FACTOR * pre_us / dec_us);
+    const double dec_bytes = (double)dec_blocks * params->n_kv_heads * 2.0 * bs * params->head_dim * 2.0;
+    // the tensor-core decode kernel (G >= 2, d = 128) runs at up to ~90 GB/s
+    // per SM; the CUDA-core one needs every SM for the HBM rate
+    const bool tc_decode = g >= 2 && params->head_dim == 128;
+    const double sm_rate = (tc_decode ? DSR_DEC_SM_GBPS : DSR_DEC_GBPS / kModelSMs) * 1e3;  // bytes/us
+    const double bw = DSR_DEC_GBPS * 1e3;
+    double t_of[kModelSMs];
+    double best_t = 1e300;
+    for (int P = 1; P < kModelSMs; ++P) {
+      const double t_pre = pre_us / P;
+      const double r1 = std::min(bw, (kModelSMs - P) * sm_rate);
+      double t = t_pre;
+      if (dec_bytes > t_pre * r1) t = t_pre + (dec_bytes - t_pre * r1) / std::min(bw, kModelSMs * sm_rate);
+      t_of[P] = t;
+      best_t = std::min(best_t, t);
+    }
+    // T(P) is flat where the decode rows hold the HBM rate throughout; take
+    // the middle of the near-optimal range, which hedges both rate estimates
+    int lo = kModelSMs, hi = 0;
+    for (int P = 1; P < kModelSMs; ++P)
+      if (t_of[P] <= best_t * 1.005) {
+        lo = std::min(lo, P);
+        hi = std::max(hi, P);
+      }
+    m->prefill_sms = (float)((lo + hi) / 2);
   }
   m->used_bytes = L.total * 4;
   int32_t* base = static_cast<int32_t*>(m->device_buf);

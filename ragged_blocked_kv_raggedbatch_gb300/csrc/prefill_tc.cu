@@ -53,6 +53,11 @@
 #define DSR_PF_REG_HIGH 200
 #endif
 static_assert(128 * DSR_PF_REG_LOW + 256 * DSR_PF_REG_HIGH <= 384 * 168, "register split over the launch budget");
+// 1: K/V tile loads carry an L2 evict_last policy (every atom of a chunk re-reads
+// its sequence's K/V prefix from L2).
+#ifndef DSR_PF_EVICT_LAST
+#define DSR_PF_EVICT_LAST 0
+#endif
 
 namespace dsr {
 
@@ -165,6 +170,12 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
       // ---------------------------------------------------------- producer
       const uint32_t box_tx = C::HALVES * C::BOX_BYTES;
       uint32_t ring = 0, vlast_uses = 0;
+#if DSR_PF_EVICT_LAST
+      const uint64_t pol = tc::policy_evict_last();
+#define DSR_PF_TMA(dst, c0, c1, b) tc::tma_load_2d_hint(dst, &pool_map, c0, c1, b, pol)
+#else
+#define DSR_PF_TMA(dst, c0, c1, b) tc::tma_load_2d(dst, &pool_map, c0, c1, b)
+#endif
       bool ok = true;
       for (int rnd = 0, k = snake_atom(0); ok && k < n_atoms; k = snake_atom(++rnd)) {
         Atom at;
@@ -197,8 +208,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
               const int krow = ((blk[i] * 2 + 0) * a.Hkv + at.c) * 64;
 #pragma unroll
               for (int h = 0; h < C::HALVES; ++h)
-                tc::tma_load_2d(kdst + h * C::KHALF + i * C::BOX_BYTES, &pool_map, h * 64, krow,
-                                &bar[B_KFULL + st]);
+                DSR_PF_TMA(kdst + h * C::KHALF + i * C::BOX_BYTES, h * 64, krow, &bar[B_KFULL + st]);
             }
           }
           // V slot free (the PV MMAs of ring step ring-2 are done)
@@ -212,7 +222,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
               const int vrow = ((blk[i] * 2 + 1) * a.Hkv + at.c) * 64;
 #pragma unroll
               for (int h = 0; h < C::HALVES; ++h)
-                tc::tma_load_2d(vdst + h * C::KHALF + i * C::BOX_BYTES, &pool_map, h * 64, vrow, vbar);
+                DSR_PF_TMA(vdst + h * C::KHALF + i * C::BOX_BYTES, h * 64, vrow, vbar);
             }
           }
           if (last_partial) {
@@ -233,6 +243,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
           }
         }
       }
+#undef DSR_PF_TMA
       if (!ok && lane == 0) set_dev_error(a.header, DS_DEVERR_WORKLIST);
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
@@ -503,6 +514,8 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // The pool as a 2-D tensor [num_blocks*2*Hkv*64 rows][D]: row
 // ((blk*2 + kv)*Hkv + head)*64 + offset; boxes of 64 rows x 64 elements with
 // 128-byte swizzle.
@@ -519,8 +532,6 @@ cudaError_t make_pool_map(CUtensorMap* map, const void* pool, const LayerArgs& a
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
-
-}  // namespace
 
 template <bool BF16, bool HALF, int D, int G>
 static cudaError_t launch_prefill_t(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
