@@ -24,10 +24,10 @@
 // The grid is persistent (one CTA per SM: three 64 KB K+V stages) and takes
 // units dynamically from a counter in the batch header, so CTAs that start late
 // -- behind a prefill grid -- simply take fewer units; the last CTA to finish
-// zeroes the counters for the next launch.  Roles (8 warps):
-//   warp 0     TMA producer: 3 stages of (K, V) tiles of 128 keys x 128 dims
-//              (128-byte-swizzled 64x64 boxes of the pool seen as a 2-D
-//              tensor); the K and V halves are refilled separately.
+// zeroes the counters for the next launch.  Roles (9 warps):
+//   warps 0, 8 TMA producers of the K and of the V halves of 3 stages of
+//              128-key x 128-dim tiles (128-byte-swizzled 64x64 boxes of the
+//              pool seen as a 2-D tensor), each half refilled once it is free.
 //   warp 1     tensor-memory owner; issues the score MMAs S(j) (one elected
 //              lane) as soon as tile j landed.
 //   warp 3     issues the value MMAs P*V(j) as soon as P(j) is written, so the
@@ -107,10 +107,10 @@ constexpr int OFF_MISC = OFF_BAR + 8 * B_COUNT;
 constexpr int SMEM = OFF_MISC + 32 + 1024;       // + room to align the base to 1024
 constexpr int TMEM_COLS = 64;
 constexpr int COL_S = 0, COL_O = 32;
-constexpr int THREADS = 256;
-// arrivals that free a unit slot: producer, the S warp's commit, the P*V
-// warp, four softmax warps
-constexpr int QEMPTY_ARRIVALS = 7;
+constexpr int THREADS = 288;
+// arrivals that free a unit slot: the two producers, the S warp's commit, the
+// P*V warp, four softmax warps
+constexpr int QEMPTY_ARRIVALS = 8;
 static_assert(SMEM <= 227 * 1024, "shared memory over the per-CTA limit");
 
 // unit record fields
@@ -184,8 +184,12 @@ __global__ void __launch_bounds__(dtc::THREADS, 1) decode_tc_kernel(
     return __all_sync(0xffffffffu, mbar_wait_bounded(&bar[b], parity));
   };
 
-  if (warp == 0) {
-    // ---------------------------------------------------------- producer
+  if (warp == 0 || warp == 8) {
+    // ---------------------------------------------------------- producers
+    // warp 0 fills the K halves of the stages, warp 8 the V halves, each as
+    // soon as its half is free, so K runs up to STAGES tiles ahead of V.
+    const int kv = warp == 8 ? 1 : 0;
+    const int b_full = kv ? B_VFULL : B_KFULL, b_empty = kv ? B_VEMPTY : B_KEMPTY;
     uint32_t k = 0, r = 0;
     bool ok = true;
 #if DSR_DTC_EVICT_FIRST
@@ -204,44 +208,32 @@ __global__ void __launch_bounds__(dtc::THREADS, 1) decode_tc_kernel(
       const int* btab = block_table + blk_off[seq];
       for (int tt = 0; tt < n_tiles; ++tt, ++r) {
         const int s = r % STAGES;
+        // this half of stage s is free once S (P*V) of tile r - STAGES is done
+        if (r >= STAGES && !warp_wait(b_empty + s, ((r / STAGES) - 1) & 1)) { ok = false; break; }
         const int b0 = b_begin + 2 * tt;
         const int nblk = min(2, b_end - b0);
-        int blk[2] = {0, 0};
-        for (int i = 0; i < nblk; ++i) {
-          blk[i] = btab[b0 + i];
-          if (blk[i] < 0 || blk[i] >= a.num_blocks) {
-            if (lane == 0) set_dev_error(hdr, DS_DEVERR_BLOCK_ID);
-            blk[i] = 0;
-          }
-        }
-        const uint32_t tx = (uint32_t)nblk * 2u * BOX_BYTES;
-        uint8_t* kdst = sm + s * STAGE_BYTES;
-        for (int kv = 0; kv < 2; ++kv) {
-          // the K (V) half of stage s is free once S (P*V) of tile r - STAGES is done
-          if (r >= STAGES && !warp_wait((kv ? B_VEMPTY : B_KEMPTY) + s, ((r / STAGES) - 1) & 1)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            uint64_t* fb = &bar[(kv ? B_VFULL : B_KFULL) + s];
-            mbar_arrive_expect_tx(fb, tx);
-            for (int i = 0; i < nblk; ++i) {
-              const int row = ((blk[i] * 2 + kv) * a.Hkv + c) * 64;
+        if (lane == 0) {
+          uint64_t* fb = &bar[b_full + s];
+          uint8_t* dst = sm + s * STAGE_BYTES + kv * KV_BYTES;
+          mbar_arrive_expect_tx(fb, (uint32_t)nblk * 2u * BOX_BYTES);
+          for (int i = 0; i < nblk; ++i) {
+            int blk = btab[b0 + i];
+            if (blk < 0 || blk >= a.num_blocks) {
+              set_dev_error(hdr, DS_DEVERR_BLOCK_ID);
+              blk = 0;
+            }
+            const int row = ((blk * 2 + kv) * a.Hkv + c) * 64;
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < 2; ++h) {
 #if DSR_DTC_EVICT_FIRST
-                tc::tma_load_2d_hint(kdst + kv * KV_BYTES + h * HALF_BYTES + i * BOX_BYTES, &pool_map, h * 64,
-                                     row, fb, pol);
+              tc::tma_load_2d_hint(dst + h * HALF_BYTES + i * BOX_BYTES, &pool_map, h * 64, row, fb, pol);
 #else
-                tc::tma_load_2d(kdst + kv * KV_BYTES + h * HALF_BYTES + i * BOX_BYTES, &pool_map, h * 64, row,
-                                fb);
+              tc::tma_load_2d(dst + h * HALF_BYTES + i * BOX_BYTES, &pool_map, h * 64, row, fb);
 #endif
-              }
             }
           }
-          __syncwarp();
         }
-        if (!ok) break;
+        __syncwarp();
       }
     }
     if (!ok) {
@@ -250,10 +242,8 @@ __global__ void __launch_bounds__(dtc::THREADS, 1) decode_tc_kernel(
     // no copy may land after the CTA's shared memory is released: wait for the
     // last fill of every stage (a phase the consumer already saw returns at once)
     if (lane == 0)
-      for (uint32_t q = (r > (uint32_t)STAGES ? r - STAGES : 0); q < r; ++q) {
-        (void)mbar_wait_bounded(&bar[B_KFULL + q % STAGES], (q / STAGES) & 1, 200000000LL);
-        (void)mbar_wait_bounded(&bar[B_VFULL + q % STAGES], (q / STAGES) & 1, 200000000LL);
-      }
+      for (uint32_t q = (r > (uint32_t)STAGES ? r - STAGES : 0); q < r; ++q)
+        (void)mbar_wait_bounded(&bar[b_full + q % STAGES], (q / STAGES) & 1, 200000000LL);
     __syncwarp();
   } else if (warp == 1 || warp == 3) {
     // ---------------------------------------------------------- MMA issuers
