@@ -42,15 +42,15 @@ def _headers():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")
+def _compile(src: str, verbose_ptxas: bool, out_dir: str = OUT_DIR, extra_flags: str = "") -> str:
+    obj = os.path.join(out_dir, os.path.basename(src) + ".o")
     newest_dep = max([os.path.getmtime(src)] + [os.path.getmtime(h) for h in _headers()])
     stamp = obj + ".flags"
-    extra = os.environ.get("DSR_NVCC_FLAGS", "")
+    extra = (os.environ.get("DSR_NVCC_FLAGS", "") + " " + extra_flags).strip()
     same_flags = os.path.exists(stamp) and open(stamp).read() == extra
     if os.path.exists(obj) and os.path.getmtime(obj) >= newest_dep and same_flags:
         return obj
-    flags = list(NVCC_FLAGS) + os.environ.get("DSR_NVCC_FLAGS", "").split()
+    flags = list(NVCC_FLAGS) + extra.split()
     if verbose_ptxas and src.endswith(".cu"):
         flags += ["-Xptxas", "-v"]
     cmd = [_nvcc()] + flags + ["-c", src, "-o", obj + ".tmp"]
@@ -65,21 +65,24 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(verbose_ptxas: bool = False, jobs: int = 0) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(verbose_ptxas: bool = False, jobs: int = 0, out_dir: str = OUT_DIR, extra_flags: str = "") -> str:
+    """Compile and link the library into out_dir (the package's _build/ by
+    default); extra_flags are added nvcc flags (e.g. a test build's -D)."""
+    os.makedirs(out_dir, exist_ok=True)
+    lib = os.path.join(out_dir, os.path.basename(LIB))
     srcs = _sources()
     jobs = jobs or min(len(srcs), max(1, os.cpu_count() or 1))
     with cf.ThreadPoolExecutor(max_workers=jobs) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
-    if os.path.exists(LIB) and os.path.getmtime(LIB) >= max(os.path.getmtime(o) for o in objs):
-        return LIB
-    tmp = LIB + ".tmp.%d" % os.getpid()
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, out_dir, extra_flags), srcs))
+    if os.path.exists(lib) and os.path.getmtime(lib) >= max(os.path.getmtime(o) for o in objs):
+        return lib
+    tmp = lib + ".tmp.%d" % os.getpid()
     cmd = [_nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

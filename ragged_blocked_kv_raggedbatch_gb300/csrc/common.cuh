@@ -185,10 +185,19 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for phase `parity` of an mbarrier, giving up after ~`limit_cycles` SM
-// cycles.  Returns false on timeout (the caller records an error and stops
-// issuing work; it never spins forever).
+// cycles (DSR_WAIT_LIMIT: ~2 s at GB300 clocks; a build with
+// -DDSR_TEST_WAIT_RUNOUT shortens it to ~1 ms so that a test can make a wait
+// run out quickly).  Returns false on timeout (the caller records an error and
+// stops issuing work; it never spins forever).
+#ifndef DSR_WAIT_LIMIT
+#ifdef DSR_TEST_WAIT_RUNOUT
+#define DSR_WAIT_LIMIT 2000000LL
+#else
+#define DSR_WAIT_LIMIT 4000000000LL
+#endif
+#endif
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  long long limit_cycles = 4000000000LL) {
+                                                  long long limit_cycles = DSR_WAIT_LIMIT) {
   if (mbar_try_wait(bar, parity)) return true;
   long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {

@@ -118,6 +118,12 @@ enum { U_UNIT = 0, U_SEQ, U_C, U_TOK, U_POS, U_BBEGIN, U_BEND, U_SLOT, U_NTILES,
 
 }  // namespace dtc
 
+#ifdef DSR_TEST_WAIT_RUNOUT
+// Test builds only: while set, the producers issue no copies, so every wait
+// on a tile runs out with nothing in flight.
+__device__ int g_test_stall_copies;
+#endif
+
 // One storage-type value (round to nearest even) as raw bits.
 template <bool BF16>
 __device__ __forceinline__ uint16_t to_bits(float x) {
@@ -212,7 +218,12 @@ __global__ void __launch_bounds__(dtc::THREADS, 1) decode_tc_kernel(
         if (r >= STAGES && !warp_wait(b_empty + s, ((r / STAGES) - 1) & 1)) { ok = false; break; }
         const int b0 = b_begin + 2 * tt;
         const int nblk = min(2, b_end - b0);
-        if (lane == 0) {
+#ifdef DSR_TEST_WAIT_RUNOUT
+        const bool stall = *reinterpret_cast<volatile int*>(&g_test_stall_copies) != 0;
+#else
+        constexpr bool stall = false;
+#endif
+        if (lane == 0 && !stall) {
           uint64_t* fb = &bar[b_full + s];
           uint8_t* dst = sm + s * STAGE_BYTES + kv * KV_BYTES;
           mbar_arrive_expect_tx(fb, (uint32_t)nblk * 2u * BOX_BYTES);
@@ -243,7 +254,7 @@ __global__ void __launch_bounds__(dtc::THREADS, 1) decode_tc_kernel(
     // last fill of every stage (a phase the consumer already saw returns at once)
     if (lane == 0)
       for (uint32_t q = (r > (uint32_t)STAGES ? r - STAGES : 0); q < r; ++q)
-        (void)mbar_wait_bounded(&bar[b_full + q % STAGES], (q / STAGES) & 1, 200000000LL);
+        (void)mbar_wait_bounded(&bar[b_full + q % STAGES], (q / STAGES) & 1, DSR_WAIT_LIMIT / 20);
     __syncwarp();
   } else if (warp == 1 || warp == 3) {
     // ---------------------------------------------------------- MMA issuers
@@ -706,3 +717,12 @@ cudaError_t launch_decode_tc(const ds_ragged_meta& m, const LayerArgs& a, const 
 }
 
 }  // namespace dsr
+
+#ifdef DSR_TEST_WAIT_RUNOUT
+// Test builds only (not part of the C ABI): stall (1) or release (0) the
+// decode producers' copies on the current device.
+extern "C" ds_status ds_test_stall_copies(int32_t on) {
+  const int v = on ? 1 : 0;
+  return cudaMemcpyToSymbol(dsr::g_test_stall_copies, &v, sizeof v) == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
+#endif
