@@ -116,6 +116,20 @@ typedef struct ds_rope_table {
     float rope_theta;
 } ds_rope_table;
 
+/* ds_ragged_meta.flags: lay every metadata region out at the offset the
+ * capacities give (not the batch's counts) and upload the whole image.  Every
+ * kernel takes its counts from the uploaded header, so with this flag the
+ * device calls make launches that depend only on the capacities: a CUDA
+ * graph captured around ds_ragged_meta_build and the layer calls for one
+ * batch replays correctly for any other batch within the capacities, once
+ * ds_ragged_meta_pack has packed that batch into the same staging buffer
+ * (ds_ragged_meta_build's validation then runs outside the graph).  The cost:
+ * an upload of the full capacity image, and launches sized by the
+ * capacities whose CTAs beyond the batch's work exit at once.  The caller
+ * keeps max_len within the rope table and the pool and workspace sized for
+ * the capacities. */
+#define DS_META_CAPACITY 1
+
 /* Ragged batch metadata (the RaggedBatchWrapper's buffers).
  * Caller fills the first group and keeps it; ds_ragged_meta_build fills the
  * rest on every batch. */
@@ -128,6 +142,7 @@ typedef struct ds_ragged_meta {
     int32_t max_seqs;
     int32_t max_tokens;
     int32_t max_blocks;   /* capacity of the packed block table              */
+    int32_t flags;        /* 0 or DS_META_CAPACITY                           */
     /* --- filled by ds_ragged_meta_build --- */
     int32_t n_seqs;
     int32_t n_tokens;
@@ -143,7 +158,9 @@ typedef struct ds_ragged_meta {
                              beside it (0: all SMs)                          */
     size_t used_bytes;    /* bytes uploaded                                  */
     /* DEVICE pointers into device_buf (int32 unless noted):
-     *   header[16]        word 0: device error bits, 1: S, 2: N, 3: blocks
+     *   header[16]        word 0: device error bits, 1: S, 2: N, 3: blocks;
+ *                     the rest are the work-list counts and the kernels'
+ *                     own counters (internal; zero after each upload)
      *   cu_seqlens[S+1]   exclusive prefix sum of new_tokens
      *   seq_seen[S], seq_new[S]
      *   blk_off[S+1]      exclusive prefix sum of ceil((seen+new)/block_size)

@@ -34,7 +34,8 @@ cudaError_t launch_rope_table(const ds_attn_params& p, int32_t max_positions, fl
   return cudaGetLastError();
 }
 
-// One CTA per packed token.  Work units of a token:
+// One CTA per packed token (CTAs past the batch's token count, in launches
+// sized by the capacities, exit at once).  Work units of a token:
 //   [0, Hkv*D/16)            rotate 16 key elements (8 pairs) -> pool K slot
 //   [.., + Hkv*D/8)          copy 8 value elements           -> pool V slot
 //   [.., + Hq*D/16) (q_out)  rotate 16 query elements        -> q_out row
@@ -43,11 +44,10 @@ __global__ void __launch_bounds__(128) append_kernel(
     const int32_t* __restrict__ tok_seq, const int32_t* __restrict__ tok_pos,
     const int32_t* __restrict__ blk_off, const int32_t* __restrict__ block_table,
     const uint16_t* __restrict__ qkv, uint16_t* __restrict__ q_out, uint16_t* __restrict__ pool,
-    const int32_t* __restrict__ skip_if_single, LayerArgs a) {
+    LayerArgs a) {
   const int t = blockIdx.x;
+  if (t >= a.header[HDR_N]) return;
   const int seq = tok_seq[t];
-  // decode rows are appended by the fused decode kernel
-  if (skip_if_single && skip_if_single[seq] == 1) return;
   const int p = tok_pos[t];
   const int W = (a.Hq + 2 * a.Hkv) * D;
   const uint16_t* row = qkv + (int64_t)t * W;
@@ -64,62 +64,55 @@ __global__ void __launch_bounds__(128) append_kernel(
   const float4* cs_row = reinterpret_cast<const float4*>(a.rope + (int64_t)p * (D / 2));
   constexpr int KU = D / 16;  // rotation units per head
   constexpr int VU = D / 8;   // copy units per head
-  const int n_k = a.Hkv * KU, n_v = a.Hkv * VU;
+  const int n_kv = a.Hkv * (KU + VU);
   const int n_q = q_out ? a.Hq * KU : 0;
-  const int total = n_k + n_v + n_q;
-  for (int u = threadIdx.x; u < total; u += blockDim.x) {
-    if (u < n_k || u >= n_k + n_v) {
-      const bool is_k = u < n_k;
-      const int uu = is_k ? u : u - n_k - n_v;
+  for (int u = threadIdx.x; u < n_kv + n_q; u += blockDim.x) {
+    if (u < n_kv) {
+      append_unit<BF16, HALF, D>(u, row, cs_row, pool, blk, off, a);
+    } else {
+      const int uu = u - n_kv;
       const int h = uu / KU, c = uu % KU;
-      const uint16_t* src = row + (is_k ? (a.Hq + h) * D : h * D);
-      int i0 = HALF ? 8 * c : 16 * c;
-      int i1 = HALF ? D / 2 + 8 * c : 16 * c + 8;
+      const uint16_t* src = row + h * D;
+      const int i0 = HALF ? 8 * c : 16 * c;
+      const int i1 = HALF ? D / 2 + 8 * c : 16 * c + 8;
       uint4 x0 = ld_nc_v4(src + i0);
       uint4 x1 = ld_nc_v4(src + i1);
       float4 cs[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) cs[q] = __ldg(cs_row + 4 * c + q);  // pairs 8c..8c+7
       rotate16<BF16, HALF>(x0, x1, cs);
-      uint16_t* dst = is_k ? pool + ((((int64_t)blk * 2 + 0) * a.Hkv + h) * kBlockSize + off) * D
-                           : q_out + (int64_t)t * a.Hq * D + h * D;
+      uint16_t* dst = q_out + (int64_t)t * a.Hq * D + h * D;
       *reinterpret_cast<uint4*>(dst + i0) = x0;
       *reinterpret_cast<uint4*>(dst + i1) = x1;
-    } else {
-      const int uu = u - n_k;
-      const int h = uu / VU, c = uu % VU;
-      uint4 v = ld_nc_v4(row + (a.Hq + a.Hkv + h) * D + 8 * c);
-      uint16_t* dst = pool + ((((int64_t)blk * 2 + 1) * a.Hkv + h) * kBlockSize + off) * D + 8 * c;
-      *reinterpret_cast<uint4*>(dst) = v;
     }
   }
 }
 
 template <bool BF16, bool HALF>
 static cudaError_t launch_append_t(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                                   void* q_out, void* pool, cudaStream_t st, bool prefill_only) {
-  dim3 grid(m.n_tokens);
-  const int32_t* skip = prefill_only ? m.seq_new : nullptr;
+                                   void* q_out, void* pool, cudaStream_t st) {
+  const int n = (m.flags & DS_META_CAPACITY) ? m.max_tokens : m.n_tokens;
+  if (n <= 0) return cudaSuccess;
+  dim3 grid(n);
   if (a.D == 128)
     append_kernel<BF16, HALF, 128><<<grid, 128, 0, st>>>(
         m.tok_seq, m.tok_pos, m.blk_off, m.block_table, static_cast<const uint16_t*>(qkv),
-        static_cast<uint16_t*>(q_out), static_cast<uint16_t*>(pool), skip, a);
+        static_cast<uint16_t*>(q_out), static_cast<uint16_t*>(pool), a);
   else
     append_kernel<BF16, HALF, 64><<<grid, 128, 0, st>>>(
         m.tok_seq, m.tok_pos, m.blk_off, m.block_table, static_cast<const uint16_t*>(qkv),
-        static_cast<uint16_t*>(q_out), static_cast<uint16_t*>(pool), skip, a);
+        static_cast<uint16_t*>(q_out), static_cast<uint16_t*>(pool), a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_append(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv, void* q_out,
-                          void* pool, cudaStream_t st, bool prefill_only) {
+                          void* pool, cudaStream_t st) {
   const bool half = a.style == DS_ROPE_HALF;
-  const bool po = prefill_only;
   if (a.dtype == DS_BF16)
-    return half ? launch_append_t<true, true>(m, a, qkv, q_out, pool, st, po)
-                : launch_append_t<true, false>(m, a, qkv, q_out, pool, st, po);
-  return half ? launch_append_t<false, true>(m, a, qkv, q_out, pool, st, po)
-              : launch_append_t<false, false>(m, a, qkv, q_out, pool, st, po);
+    return half ? launch_append_t<true, true>(m, a, qkv, q_out, pool, st)
+                : launch_append_t<true, false>(m, a, qkv, q_out, pool, st);
+  return half ? launch_append_t<false, true>(m, a, qkv, q_out, pool, st)
+              : launch_append_t<false, false>(m, a, qkv, q_out, pool, st);
 }
 
 }  // namespace dsr

@@ -21,6 +21,15 @@ enum : int {
   HDR_BLOCKS = 3,
   HDR_DEC_NEXT = 4,  // decode units handed out so far (tensor-core decode kernel)
   HDR_DEC_DONE = 5,  // its CTAs that finished; the last one zeroes both words
+  // Counts the kernels read here rather than from launch arguments, so that
+  // launches sized by the capacities serve any batch within them.
+  HDR_PRE_TILES = 6,  // prefill tiles (atoms = tiles x KV heads)
+  HDR_DEC_ITEMS = 7,  // decode split items
+  HDR_DEC_SEQS = 8,   // decode rows
+  HDR_SPLIT = 9,      // KV blocks per decode split
+  HDR_PRE_CTAS = 10,  // CTAs of the prefill grid that work (0: one per SM)
+  HDR_PRE_BAR = 11,   // fused prefill: CTAs past the append prologue
+  HDR_PRE_DONE = 12,  // fused prefill: CTAs finished; the last one zeroes 11, 12
   HDR_WORDS = 16,
 };
 
@@ -28,6 +37,13 @@ constexpr int kBlockSize = 64;        // tokens per KV block (only supported val
 constexpr int kPrefillRows = 256;     // rows (tokens x heads of one KV group) per prefill atom
 constexpr int kMinSplitBlocks = 4;    // smallest decode split, in KV blocks
 constexpr int kMaxSplitBlocks = 32;   // largest decode split, in KV blocks
+
+// Upper bounds of the work lists for given capacities (tiles of up to 256/G
+// tokens, splits of at least kMinSplitBlocks blocks).
+inline int64_t max_prefill_tiles(int64_t max_seqs, int64_t max_tokens) { return max_seqs + max_tokens; }
+inline int64_t max_decode_items(int64_t max_seqs, int64_t max_blocks) {
+  return max_seqs + (max_blocks + kMinSplitBlocks - 1) / kMinSplitBlocks;
+}
 
 // Split-decode partials in a workspace: the (m, l) pairs [items][Hq][2],
 // then o [items][Hq][D] from the next 256-byte boundary, so that the float4
@@ -47,8 +63,7 @@ struct LayerArgs {
   int32_t num_blocks;      // pool size
   int32_t max_positions;   // rotary table rows
   const float2* rope;      // [max_positions][D/2]
-  int32_t* header;         // device error word lives at header[HDR_ERR]
-  int32_t split_blocks;    // KV blocks per decode split
+  int32_t* header;         // device error word at header[HDR_ERR], counts at HDR_*
 };
 
 // ----------------------------------------------------------- device helpers --
@@ -225,6 +240,37 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   return r;
 }
 
+// One unit of the KV append for packed token t at position p (sequence block
+// blk, slot off): units [0, Hkv*D/16) rotate 16 key elements (8 pairs) into
+// the pool's K slot; units [Hkv*D/16, Hkv*(D/16 + D/8)) copy 8 value elements
+// into its V slot.  row: the token's qkv row; cs_row: its rotary table row.
+template <bool BF16, bool HALF, int D>
+__device__ __forceinline__ void append_unit(int u, const uint16_t* row, const float4* cs_row,
+                                            uint16_t* pool, int blk, int off, const LayerArgs& a) {
+  constexpr int KU = D / 16, VU = D / 8;
+  const int n_k = a.Hkv * KU;
+  if (u < n_k) {
+    const int h = u / KU, c = u % KU;
+    const uint16_t* src = row + (a.Hq + h) * D;
+    const int i0 = HALF ? 8 * c : 16 * c;
+    const int i1 = HALF ? D / 2 + 8 * c : 16 * c + 8;
+    uint4 x0 = ld_nc_v4(src + i0);
+    uint4 x1 = ld_nc_v4(src + i1);
+    float4 cs[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cs[q] = __ldg(cs_row + 4 * c + q);  // pairs 8c..8c+7
+    rotate16<BF16, HALF>(x0, x1, cs);
+    uint16_t* dst = pool + ((((int64_t)blk * 2 + 0) * a.Hkv + h) * kBlockSize + off) * D;
+    *reinterpret_cast<uint4*>(dst + i0) = x0;
+    *reinterpret_cast<uint4*>(dst + i1) = x1;
+  } else {
+    const int uu = u - n_k;
+    const int h = uu / VU, c = uu % VU;
+    const uint4 v = ld_nc_v4(row + (a.Hq + a.Hkv + h) * D + 8 * c);
+    *reinterpret_cast<uint4*>(pool + ((((int64_t)blk * 2 + 1) * a.Hkv + h) * kBlockSize + off) * D + 8 * c) = v;
+  }
+}
+
 #endif  // __CUDACC__
 
 // Records the message ds_last_error() returns on this thread (host.cpp).
@@ -234,10 +280,11 @@ void set_last_error(const char* msg);
 // Implemented in the .cu files; called by the host layer after validation.
 cudaError_t launch_rope_table(const ds_attn_params& p, int32_t max_positions, float2* table,
                               cudaStream_t st);
-// prefill_only: tokens of decode rows (sequences with one new token) are left
-// to the fused decode kernel.
+// Launches are sized by the batch's counts, or by the capacities when
+// m.flags has DS_META_CAPACITY (the kernels read the batch's counts from the
+// uploaded header and their surplus CTAs exit at once).
 cudaError_t launch_append(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                          void* q_out, void* pool, cudaStream_t st, bool prefill_only = false);
+                          void* q_out, void* pool, cudaStream_t st);
 // overlap_previous: launch as a programmatic dependent of the kernel before it
 // on the stream (the prefill kernel), so decode CTAs can start while it runs.
 // fused_append: the kernel also appends each decode row's new K/V (the append
@@ -249,6 +296,8 @@ cudaError_t launch_decode(const ds_ragged_meta& m, const LayerArgs& a, const voi
                           const void* pool, void* out, float* ws, cudaStream_t st,
                           bool overlap_previous, bool fused_append = false,
                           int32_t* counters = nullptr);
+// True when launch_decode runs the layer's decode rows on the tensor-core kernel.
+bool decode_on_tensor_cores(const LayerArgs& a);
 // Decode rows of grouped-query layers (G >= 2, D = 128) on the tensor cores;
 // the same arguments and results as launch_decode (decode_tc.cu).
 cudaError_t launch_decode_tc(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
@@ -257,7 +306,10 @@ cudaError_t launch_decode_tc(const ds_ragged_meta& m, const LayerArgs& a, const 
 // The merge of the split partials of multi-split decode rows (decode.cu).
 cudaError_t launch_decode_combine(const ds_ragged_meta& m, const LayerArgs& a, const float* ws,
                                   void* out, cudaStream_t st);
+// fused_append: the prefill CTAs first append the prefill chunks' new K/V
+// (rotated) to the pool, meet at a grid barrier (cooperative launch), then run
+// the atoms; decode rows are left to the fused decode kernel.
 cudaError_t launch_prefill(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                           const void* pool, void* out, cudaStream_t st);
+                           void* pool, void* out, cudaStream_t st, bool fused_append = false);
 
 }  // namespace dsr

@@ -106,8 +106,11 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 4 ? DSR_DECODE_MINB_GQA : DSR
     const int32_t* __restrict__ seq_seen, const int32_t* __restrict__ blk_off,
     const int32_t* __restrict__ block_table, const uint16_t* __restrict__ qkv,
     uint16_t* __restrict__ pool, uint16_t* __restrict__ out, float* __restrict__ ws,
-    int32_t* __restrict__ counters, int32_t n_items, LayerArgs a) {
+    int32_t* __restrict__ counters, LayerArgs a) {
   using C = DecodeCfg<BF16, HALF, D, G, WARPS, STAGES>;
+  // the batch's split items (a launch sized by the capacities has more CTAs)
+  const int n_items = a.header[HDR_DEC_ITEMS];
+  if ((int)blockIdx.x >= n_items) return;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -453,7 +456,7 @@ __global__ void __launch_bounds__(WARPS * 32, G >= 4 ? DSR_DECODE_MINB_GQA : DSR
   if (FUSED && counters != nullptr && slot >= 0) {
     // ---- the last split of (row, KV head c) to finish merges all partials
     __shared__ int s_last;
-    const int split = a.split_blocks;
+    const int split = a.header[HDR_SPLIT];
     const int cnt = (nb + split - 1) / split;
     const int first = slot - b_begin / split;  // a row's splits hold consecutive slots
     // every thread's partials precede thread 0's fence (barrier), which
@@ -499,11 +502,12 @@ template <bool BF16, int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const int4* __restrict__ dseqs,
                                                              const float* __restrict__ ws,
                                                              uint16_t* __restrict__ out,
-                                                             int32_t n_items, int32_t Hq) {
+                                                             const int32_t* __restrict__ header, int32_t Hq) {
   constexpr int DPL = D / 32;  // dims per lane: 4 or 2
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
-  if (h >= Hq) return;
+  if (h >= Hq || (int)blockIdx.x >= header[HDR_DEC_SEQS]) return;
+  const int n_items = header[HDR_DEC_ITEMS];
   const int4 ds = dseqs[blockIdx.x];
   const int t = ds.y, first = ds.z, cnt = ds.w;
   if (cnt <= 1) return;
@@ -546,7 +550,9 @@ static cudaError_t launch_decode_t(const ds_ragged_meta& m, const LayerArgs& a, 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(m.n_decode_items, a.Hkv);
+  const int64_t items = (m.flags & DS_META_CAPACITY) ? max_decode_items(m.max_seqs, m.max_blocks)
+                                                      : m.n_decode_items;
+  cfg.gridDim = dim3((unsigned)items, a.Hkv);
   cfg.blockDim = dim3(WARPS * 32);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = st;
@@ -563,25 +569,26 @@ static cudaError_t launch_decode_t(const ds_ragged_meta& m, const LayerArgs& a, 
   e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const int4*>(m.decode_items), m.cu_seqlens,
                          m.seq_seen, m.blk_off, m.block_table, static_cast<const uint16_t*>(qkv),
                          static_cast<uint16_t*>(const_cast<void*>(pool)), static_cast<uint16_t*>(out), ws,
-                         counters, (int32_t)m.n_decode_items, a);
+                         counters, a);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (counters == nullptr && m.n_decode_items > m.n_decode_seqs) e = launch_decode_combine(m, a, ws, out, st);
+  if (counters == nullptr && ((m.flags & DS_META_CAPACITY) || m.n_decode_items > m.n_decode_seqs))
+    e = launch_decode_combine(m, a, ws, out, st);
   return e;
 }
 
 cudaError_t launch_decode_combine(const ds_ragged_meta& m, const LayerArgs& a, const float* ws,
                                   void* out, cudaStream_t st) {
-  dim3 g2(m.n_decode_seqs, (a.Hq + 3) / 4);
+  dim3 g2((m.flags & DS_META_CAPACITY) ? m.max_seqs : m.n_decode_seqs, (a.Hq + 3) / 4);
   const int4* dseqs = reinterpret_cast<const int4*>(m.decode_seqs);
   uint16_t* o = static_cast<uint16_t*>(out);
   if (a.dtype == DS_BF16) {
-    if (a.D == 128) decode_combine_kernel<true, 128><<<g2, 128, 0, st>>>(dseqs, ws, o, m.n_decode_items, a.Hq);
-    else decode_combine_kernel<true, 64><<<g2, 128, 0, st>>>(dseqs, ws, o, m.n_decode_items, a.Hq);
+    if (a.D == 128) decode_combine_kernel<true, 128><<<g2, 128, 0, st>>>(dseqs, ws, o, m.header, a.Hq);
+    else decode_combine_kernel<true, 64><<<g2, 128, 0, st>>>(dseqs, ws, o, m.header, a.Hq);
   } else {
-    if (a.D == 128) decode_combine_kernel<false, 128><<<g2, 128, 0, st>>>(dseqs, ws, o, m.n_decode_items, a.Hq);
-    else decode_combine_kernel<false, 64><<<g2, 128, 0, st>>>(dseqs, ws, o, m.n_decode_items, a.Hq);
+    if (a.D == 128) decode_combine_kernel<false, 128><<<g2, 128, 0, st>>>(dseqs, ws, o, m.header, a.Hq);
+    else decode_combine_kernel<false, 64><<<g2, 128, 0, st>>>(dseqs, ws, o, m.header, a.Hq);
   }
   return cudaGetLastError();
 }
@@ -607,14 +614,14 @@ static cudaError_t launch_decode_d(const ds_ragged_meta& m, const LayerArgs& a, 
                     : launch_decode_g<BF16, HALF, 64>(m, a, qkv, pool, out, ws, st, ov, fu, cnt);
 }
 
+bool decode_on_tensor_cores(const LayerArgs& a) { return DSR_DECODE_TC && a.D == 128 && a.G >= 2; }
+
 cudaError_t launch_decode(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
                           const void* pool, void* out, float* ws, cudaStream_t st,
                           bool overlap_previous, bool fused_append, int32_t* counters) {
-#if DSR_DECODE_TC
   // grouped-query rows of head size 128: the tensor-core kernel (decode_tc.cu)
-  if (a.D == 128 && a.G >= 2)
+  if (decode_on_tensor_cores(a))
     return launch_decode_tc(m, a, qkv, pool, out, ws, st, overlap_previous, fused_append, counters);
-#endif
   const bool half = a.style == DS_ROPE_HALF;
   const bool ov = overlap_previous, fu = fused_append;
   if (a.dtype == DS_BF16)

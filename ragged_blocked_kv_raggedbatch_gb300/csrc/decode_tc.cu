@@ -24,7 +24,7 @@
 // The grid is persistent (one CTA per SM: three 64 KB K+V stages) and takes
 // units dynamically from a counter in the batch header, so CTAs that start late
 // -- behind a prefill grid -- simply take fewer units; the last CTA to finish
-// zeroes the counters for the next launch.  Roles (9 warps):
+// zeroes the counters for the next launch.  Roles (10 warps):
 //   warps 0, 8 TMA producers of the K and of the V halves of 3 stages of
 //              128-key x 128-dim tiles (128-byte-swizzled 64x64 boxes of the
 //              pool seen as a 2-D tensor), each half refilled once it is free.
@@ -45,6 +45,8 @@
 //              zero the V rows past the last key of a partial tile (those slots
 //              may hold anything and 0 * NaN would poison P*V); epilogue O / l
 //              -> out, or (m, l, O) partials for the combine step.
+//   warp 9     (fused variant with counters) counts each finished split done
+//              and merges a row's partials when its last split finishes.
 // Tensor memory (64 columns): S[2] at 0 / 16, O[2] at 32 / 48.
 // Every mbarrier wait is bounded: on timeout the CTA records an error and stops.
 #include <algorithm>
@@ -100,14 +102,19 @@ enum {
   B_PFULL = B_SFULL + 2,
   B_ODONE = B_PFULL + 2,
   B_MMADRAIN = B_ODONE + 2,  // one per MMA warp
-  B_COUNT = B_MMADRAIN + 2
+  B_MFULL = B_MMADRAIN + 2,  // merge records (fused decode with counters)
+  B_MEMPTY = B_MFULL + 4,
+  B_COUNT = B_MEMPTY + 4
 };
-// tensor-memory address, merge flag
+constexpr int MQ = 4;          // merge-record slots
+constexpr int MREC_INTS = 8;
+// tensor-memory address; then the merge records
 constexpr int OFF_MISC = OFF_BAR + 8 * B_COUNT;
-constexpr int SMEM = OFF_MISC + 32 + 1024;       // + room to align the base to 1024
+constexpr int OFF_MREC = OFF_MISC + 16;
+constexpr int SMEM = OFF_MREC + MQ * MREC_INTS * 4 + 1024;  // + room to align the base to 1024
 constexpr int TMEM_COLS = 64;
 constexpr int COL_S = 0, COL_O = 32;
-constexpr int THREADS = 288;
+constexpr int THREADS = 320;
 // arrivals that free a unit slot: the two producers, the S warp's commit, the
 // P*V warp, four softmax warps
 constexpr int QEMPTY_ARRIVALS = 8;
@@ -141,7 +148,7 @@ __global__ void __launch_bounds__(dtc::THREADS, 1) decode_tc_kernel(
     const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ seq_seen,
     const int32_t* __restrict__ blk_off, const int32_t* __restrict__ block_table,
     const uint16_t* __restrict__ qkv, uint16_t* __restrict__ pool, uint16_t* __restrict__ out,
-    float* __restrict__ ws, int32_t* __restrict__ counters, int32_t n_items, LayerArgs a) {
+    float* __restrict__ ws, int32_t* __restrict__ counters, LayerArgs a) {
   using namespace dtc;
   static_assert(G >= 2 && G <= 8, "head group");
   extern __shared__ uint8_t smem_raw[];
@@ -149,12 +156,13 @@ __global__ void __launch_bounds__(dtc::THREADS, 1) decode_tc_kernel(
   uint8_t* sm = smem_raw + (((raw_u + 1023u) & ~1023u) - raw_u);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
-  int* merge_flag = reinterpret_cast<int*>(sm + OFF_MISC + 4);
+  int* mrec = reinterpret_cast<int*>(sm + OFF_MREC);
   int* info = reinterpret_cast<int*>(sm + OFF_INFO);
   float* red = reinterpret_cast<float*>(sm + OFF_RED);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_units = n_items * a.Hkv;
   int32_t* hdr = a.header;
+  const int n_items = hdr[HDR_DEC_ITEMS];
+  const int n_units = n_items * a.Hkv;
 
   // Q slots and P buffers start at zero: their rows G..15 are never written.
   for (int i = tid; i < (QN + 2) * QP_BYTES / 16; i += THREADS)
@@ -178,6 +186,10 @@ __global__ void __launch_bounds__(dtc::THREADS, 1) decode_tc_kernel(
     }
     mbar_init(&bar[B_MMADRAIN], 1);
     mbar_init(&bar[B_MMADRAIN + 1], 1);
+    for (int s = 0; s < MQ; ++s) {
+      mbar_init(&bar[B_MFULL + s], 4);  // the four softmax warps
+      mbar_init(&bar[B_MEMPTY + s], 1);
+    }
     fence_barrier_init();
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, TMEM_COLS);
@@ -430,7 +442,7 @@ __global__ void __launch_bounds__(dtc::THREADS, 1) decode_tc_kernel(
       if (lane == 0) tc::mbar_arrive(&bar[B_QFULL + slot]);
       ++k;
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------- softmax
     // The four warps synchronise on named barrier 1.  A named barrier waits
     // without a bound, so no warp may leave the common sequence of barriers on
@@ -445,7 +457,7 @@ __global__ void __launch_bounds__(dtc::THREADS, 1) decode_tc_kernel(
     auto wwait = [&](int b, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait_bounded(&bar[b], parity));
     };
-    uint32_t k = 0, jg = 0, xc = 0;
+    uint32_t k = 0, jg = 0, xc = 0, mq = 0;
     bool wok = true, ok = true;
     while (true) {
       const int slot = k % QN;
@@ -596,42 +608,93 @@ __global__ void __launch_bounds__(dtc::THREADS, 1) decode_tc_kernel(
           }
         }
         if (FUSED && counters != nullptr) {
-          // the last split of (row, KV head c) to finish merges all partials
-          // (the combine kernel's arithmetic, in its order)
-          const int split = a.split_blocks;
-          const int nb = (pos + 1 + 63) / 64;
-          const int cnt = (nb + split - 1) / split;
-          const int first = wslot - b_begin / split;  // a row's splits hold consecutive slots
-          tc::bar_sync(1, 128);  // every thread's partials precede thread 0's fence
+          // hand the unit to the merge warp, which counts it done and, for
+          // the last split of (row, KV head c), merges all partials; the
+          // softmax warps go on with the next unit meanwhile
+          const int q = mq % MQ;
+          if (mq >= MQ) wok = wok && wwait(B_MEMPTY + q, ((mq / MQ) - 1) & 1);
           if (ts == 0) {
-            __threadfence();
-            *merge_flag = atomicAdd(&counters[seq * a.Hkv + c], 1) == cnt - 1;
+            int* r = mrec + q * MREC_INTS;
+            r[0] = seq;
+            r[1] = c;
+            r[2] = wslot;
+            r[3] = t;
+            r[4] = pos;
+            r[5] = b_begin;
           }
-          tc::bar_sync(1, 128);
-          if (*merge_flag) {
-            __threadfence();
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              const int hq = c * G + h;
-              float M = -1.0e30f;
-              for (int q = 0; q < cnt; ++q) M = fmaxf(M, __ldcg(ws + ((int64_t)(first + q) * a.Hq + hq) * 2));
-              float acc = 0.f, lt = 0.f;
-              for (int q = 0; q < cnt; ++q) {
-                const float* ml = ws + ((int64_t)(first + q) * a.Hq + hq) * 2;
-                const float scl = fast_exp2(__ldcg(ml) - M);
-                lt += scl * __ldcg(ml + 1);
-                acc += scl * __ldcg(wo + ((int64_t)(first + q) * a.Hq + hq) * D + ts);
-              }
-              out[(int64_t)t * a.Hq * D + hq * D + ts] = to_bits<BF16>(acc * (1.f / lt));
-            }
-            if (ts == 0) counters[seq * a.Hkv + c] = 0;  // ready for the next launch
-          }
+          ++mq;
+          __syncwarp();  // this warp's partials and (lane 0 of warp 4) the record
+          if (lane == 0) tc::mbar_arrive(&bar[B_MFULL + q]);
         }
       }
-      // the row-sum and merge-flag scratch is reused by the next unit
+      // the row-sum scratch is reused by the next unit
       tc::bar_sync(1, 128);
     }
     if (!ok) set_dev_error(hdr, DS_DEVERR_WORKLIST);
+    if (FUSED && counters != nullptr) {
+      // end of the merge warp's records (bounded: the slot's previous record
+      // may still be in use)
+      const int q = mq % MQ;
+      if (mq >= MQ) (void)wwait(B_MEMPTY + q, ((mq / MQ) - 1) & 1);
+      if (ts == 0) mrec[q * MREC_INTS] = -1;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar[B_MFULL + q]);
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------- merge warp
+    // (fused decode with counters) for each multi-split unit the softmax warps
+    // finished: publish its partials (this fence is cumulative: it covers the
+    // softmax threads' writes this warp acquired through the record's
+    // barrier), count it done on the (row, KV head) counter, and if it is the
+    // last split, merge every split's partials (the combine kernel's
+    // arithmetic, in its order) into the output row and reset the counter.
+    if (FUSED && counters != nullptr) {
+      for (uint32_t i = 0;; ++i) {
+        const int q = i % MQ;
+        if (!warp_wait(B_MFULL + q, (i / MQ) & 1)) {
+          if (lane == 0) set_dev_error(hdr, DS_DEVERR_WORKLIST);
+          break;
+        }
+        const int* r = mrec + q * MREC_INTS;
+        const int seq = r[0], c = r[1], wslot = r[2], t = r[3], pos = r[4], b_begin = r[5];
+        __syncwarp();
+        if (seq < 0) break;
+        const int split = hdr[HDR_SPLIT];
+        const int nb = (pos + 1 + 63) / 64;
+        const int cnt = (nb + split - 1) / split;
+        const int first = wslot - b_begin / split;  // a row's splits hold consecutive slots
+        int last = 0;
+        if (lane == 0) {
+          __threadfence();
+          last = atomicAdd(&counters[seq * a.Hkv + c], 1) == cnt - 1;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+          const float* wo = ws + ws_o_offset(n_items, a.Hq);
+          for (int h = 0; h < G; ++h) {
+            const int hq = c * G + h;
+            float M = -1.0e30f;
+            for (int k2 = 0; k2 < cnt; ++k2) M = fmaxf(M, __ldcg(ws + ((int64_t)(first + k2) * a.Hq + hq) * 2));
+            float acc[4] = {0.f, 0.f, 0.f, 0.f}, lt = 0.f;
+            for (int k2 = 0; k2 < cnt; ++k2) {
+              const float* ml = ws + ((int64_t)(first + k2) * a.Hq + hq) * 2;
+              const float scl = fast_exp2(__ldcg(ml) - M);
+              lt += scl * __ldcg(ml + 1);
+              const float* src = wo + ((int64_t)(first + k2) * a.Hq + hq) * D;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[e] += scl * __ldcg(src + lane + 32 * e);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              out[(int64_t)t * a.Hq * D + hq * D + lane + 32 * e] = to_bits<BF16>(acc[e] * (1.f / lt));
+          }
+          if (lane == 0) counters[seq * a.Hkv + c] = 0;  // ready for the next launch
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[B_MEMPTY + q]);
+      }
+    }
   }
 
   tc::fence_before();
@@ -666,7 +729,9 @@ static cudaError_t launch_dtc_t(const ds_ragged_meta& m, const LayerArgs& a, con
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int64_t units = (int64_t)m.n_decode_items * a.Hkv;
+  // persistent: one CTA per SM, fewer for a small batch (unless the launch
+  // must serve any batch within the capacities)
+  const int64_t units = (m.flags & DS_META_CAPACITY) ? (int64_t)sms : (int64_t)m.n_decode_items * a.Hkv;
   const int cap = DSR_DTC_MAX_CTAS > 0 ? std::min(sms, DSR_DTC_MAX_CTAS) : sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>(units, cap)));
@@ -684,11 +749,12 @@ static cudaError_t launch_dtc_t(const ds_ragged_meta& m, const LayerArgs& a, con
   e = cudaLaunchKernelEx(&cfg, kern, map, reinterpret_cast<const int4*>(m.decode_items), m.cu_seqlens,
                          m.seq_seen, m.blk_off, m.block_table, static_cast<const uint16_t*>(qkv),
                          static_cast<uint16_t*>(const_cast<void*>(pool)), static_cast<uint16_t*>(out), ws,
-                         counters, (int32_t)m.n_decode_items, a);
+                         counters, a);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (counters == nullptr && m.n_decode_items > m.n_decode_seqs) e = launch_decode_combine(m, a, ws, out, st);
+  if (counters == nullptr && ((m.flags & DS_META_CAPACITY) || m.n_decode_items > m.n_decode_seqs))
+    e = launch_decode_combine(m, a, ws, out, st);
   return e;
 }
 

@@ -75,11 +75,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // to the device's real count.
 constexpr int kModelSMs = 152;
 
-// Upper bounds of the work lists for given capacities.
-int64_t max_prefill_tiles(int64_t max_seqs, int64_t max_tokens) { return max_seqs + max_tokens; }
-int64_t max_decode_items(int64_t max_seqs, int64_t max_blocks) {
-  return max_seqs + (max_blocks + dsr::kMinSplitBlocks - 1) / dsr::kMinSplitBlocks;
-}
+using dsr::max_decode_items;
+using dsr::max_prefill_tiles;
 
 // Words (int32) of the packed metadata for the given counts.
 struct Layout {
@@ -127,7 +124,6 @@ dsr::LayerArgs layer_args(const ds_ragged_meta* m, const ds_attn_params* p,
   a.max_positions = r->max_positions;
   a.rope = static_cast<const float2*>(r->table);
   a.header = m->header;
-  a.split_blocks = m->split_blocks;
   return a;
 }
 
@@ -271,7 +267,12 @@ ds_status ds_ragged_meta_pack(const ds_seq_desc* seqs, int32_t n_seqs,
     n_items += (nb + split - 1) / split;
   }
 
-  Layout L = layout_for(n_seqs, N, B, pre_tiles, n_items, n_dec);
+  // capacity layout: every region at the offset the capacities give, so the
+  // device pointers are the same for every batch packed into this buffer
+  const bool cap = (m->flags & DS_META_CAPACITY) != 0;
+  Layout L = cap ? layout_for(m->max_seqs, m->max_tokens, m->max_blocks, max_prefill_tiles(m->max_seqs, m->max_tokens),
+                              max_decode_items(m->max_seqs, m->max_blocks), m->max_seqs)
+                 : layout_for(n_seqs, N, B, pre_tiles, n_items, n_dec);
   int32_t* w = static_cast<int32_t*>(m->host_staging);
   // Every region below is written in full; only the header and the alignment
   // words before the work lists need clearing.
@@ -401,6 +402,11 @@ ds_status ds_ragged_meta_pack(const ds_seq_desc* seqs, int32_t n_seqs,
       }
     m->prefill_sms = (float)((lo + hi) / 2);
   }
+  w[L.hdr + dsr::HDR_PRE_TILES] = (int32_t)tv.size();
+  w[L.hdr + dsr::HDR_DEC_ITEMS] = (int32_t)n_items;
+  w[L.hdr + dsr::HDR_DEC_SEQS] = n_dec;
+  w[L.hdr + dsr::HDR_SPLIT] = split;
+  w[L.hdr + dsr::HDR_PRE_CTAS] = (int32_t)std::ceil(m->prefill_sms);
   m->used_bytes = L.total * 4;
   int32_t* base = static_cast<int32_t*>(m->device_buf);
   m->header = base + L.hdr;
@@ -459,7 +465,8 @@ ds_status ds_kv_rotary_append(const ds_ragged_meta* meta, const ds_attn_params* 
                               const ds_kv_pool* pool, void* stream) {
   if (ds_status s = check_params(params)) return s;
   if (ds_status s = check_meta(meta)) return s;
-  if (meta->n_tokens == 0) return DS_OK;
+  const bool cap = (meta->flags & DS_META_CAPACITY) != 0;
+  if (meta->n_tokens == 0 && !cap) return DS_OK;
   if (ds_status s = check_rope(rope, params, meta)) return s;
   if (ds_status s = check_pool(pool, meta)) return s;
   if (!qkv || !aligned(qkv, 16)) return fail(DS_ERR_INVALID_ARG, "qkv NULL or not 16-byte aligned");
@@ -481,18 +488,26 @@ ds_status ds_blocked_attention_workspace_size(const ds_attn_params* params, int3
   return DS_OK;
 }
 
+// Split items a call must have workspace for: the batch's, or the capacities'
+// when the launches must serve any batch within them.
+static int64_t ws_items(const ds_ragged_meta* m) {
+  return (m->flags & DS_META_CAPACITY) ? max_decode_items(m->max_seqs, m->max_blocks) : m->n_decode_items;
+}
+
 ds_status ds_blocked_attention(const ds_ragged_meta* meta, const ds_attn_params* params,
                                const ds_rope_table* rope, const void* qkv, const ds_kv_pool* pool,
                                void* out, void* workspace, size_t ws_bytes, void* stream) {
   if (ds_status s = check_params(params)) return s;
   if (ds_status s = check_meta(meta)) return s;
-  if (meta->n_tokens == 0) return DS_OK;
+  const bool cap = (meta->flags & DS_META_CAPACITY) != 0;
+  if (meta->n_tokens == 0 && !cap) return DS_OK;
   if (ds_status s = check_rope(rope, params, meta)) return s;
   if (ds_status s = check_pool(pool, meta)) return s;
   if (!qkv || !aligned(qkv, 16)) return fail(DS_ERR_INVALID_ARG, "qkv NULL or not 16-byte aligned");
   if (!out || !aligned(out, 16)) return fail(DS_ERR_INVALID_ARG, "out NULL or not 16-byte aligned");
-  const size_t need = (size_t)dsr::ws_partial_bytes(meta->n_decode_items, params->n_q_heads, params->head_dim);
-  if (meta->n_decode_items > 0) {
+  const int64_t items = ws_items(meta);
+  const size_t need = (size_t)dsr::ws_partial_bytes(items, params->n_q_heads, params->head_dim);
+  if (items > 0) {
     if (!workspace || !aligned(workspace, 256))
       return fail(DS_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
     if (ws_bytes < need)
@@ -500,13 +515,13 @@ ds_status ds_blocked_attention(const ds_ragged_meta* meta, const ds_attn_params*
   }
   dsr::LayerArgs a = layer_args(meta, params, rope, pool->num_blocks);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (meta->n_prefill_tiles > 0) {
+  const bool pre = cap || meta->n_prefill_tiles > 0;
+  if (pre) {
     cudaError_t e = dsr::launch_prefill(*meta, a, qkv, pool->base, out, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill kernel");
   }
-  if (meta->n_decode_items > 0) {
-    cudaError_t e = dsr::launch_decode(*meta, a, qkv, pool->base, out, static_cast<float*>(workspace), st,
-                                       meta->n_prefill_tiles > 0);
+  if (cap || meta->n_decode_items > 0) {
+    cudaError_t e = dsr::launch_decode(*meta, a, qkv, pool->base, out, static_cast<float*>(workspace), st, pre);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernels");
   }
   return DS_OK;
@@ -553,15 +568,16 @@ ds_status ds_fused_append_attention(const ds_ragged_meta* meta, const ds_attn_pa
                                     size_t ws_bytes, void* stream) {
   if (ds_status s = check_params(params)) return s;
   if (ds_status s = check_meta(meta)) return s;
-  if (meta->n_tokens == 0) return DS_OK;
+  const bool cap = (meta->flags & DS_META_CAPACITY) != 0;
+  if (meta->n_tokens == 0 && !cap) return DS_OK;
   if (ds_status s = check_rope(rope, params, meta)) return s;
   if (ds_status s = check_pool(pool, meta)) return s;
   if (!qkv || !aligned(qkv, 16)) return fail(DS_ERR_INVALID_ARG, "qkv NULL or not 16-byte aligned");
   if (!out || !aligned(out, 16)) return fail(DS_ERR_INVALID_ARG, "out NULL or not 16-byte aligned");
   const size_t cb = fused_counter_bytes(params, meta->max_seqs);
-  const size_t need = cb + (size_t)dsr::ws_partial_bytes(meta->n_decode_items, params->n_q_heads,
-                                                          params->head_dim);
-  if (meta->n_decode_items > 0) {
+  const int64_t items = ws_items(meta);
+  const size_t need = cb + (size_t)dsr::ws_partial_bytes(items, params->n_q_heads, params->head_dim);
+  if (items > 0) {
     if (!workspace || !aligned(workspace, 256))
       return fail(DS_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
     if (ws_bytes < need)
@@ -569,25 +585,25 @@ ds_status ds_fused_append_attention(const ds_ragged_meta* meta, const ds_attn_pa
   }
   dsr::LayerArgs a = layer_args(meta, params, rope, pool->num_blocks);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (meta->n_prefill_seqs > 0) {
-    cudaError_t e = dsr::launch_append(*meta, a, qkv, nullptr, pool->base, st, /*prefill_only=*/true);
-    if (e != cudaSuccess) return cuda_fail(e, "append kernel");
-  }
-  if (meta->n_prefill_tiles > 0) {
-    cudaError_t e = dsr::launch_prefill(*meta, a, qkv, pool->base, out, st);
+  // prefill chunks: their K/V append is the prefill kernel's prologue
+  const bool pre = cap || meta->n_prefill_tiles > 0;
+  if (pre) {
+    cudaError_t e = dsr::launch_prefill(*meta, a, qkv, pool->base, out, st, /*fused_append=*/true);
     if (e != cudaSuccess) return cuda_fail(e, "prefill kernel");
   }
-  if (meta->n_decode_items > 0) {
-    // Merge split partials inside the decode kernel (the decode rows are then
-    // one launch) while its grid is at most two waves of 3 CTAs per SM.  On a
-    // larger grid the separate merge launch costs less than holding every CTA
-    // for its count: decode-only batch of 256 rows on GB300, 1.304 ms merged in
-    // the kernel against 1.297 ms with the merge kernel.
-    const bool merge_in_kernel =
-        (int64_t)meta->n_decode_items * params->n_kv_heads <= 6LL * device_sm_count();
+  if (cap || meta->n_decode_items > 0) {
+    // Decode rows append their own K/V.  Their split partials are merged
+    // inside the decode kernel by the tensor-core kernel, and by the CUDA-core
+    // one while its grid is at most two waves of 3 CTAs per SM (on a larger
+    // grid the separate merge launch costs less than holding every CTA for its
+    // count: decode-only batch of 256 rows on GB300, 1.304 ms merged in the
+    // kernel against 1.297 ms with the merge kernel), and always in a launch
+    // that must serve any batch within the capacities.
+    const bool merge_in_kernel = cap || dsr::decode_on_tensor_cores(a) ||
+                                 (int64_t)meta->n_decode_items * params->n_kv_heads <= 6LL * device_sm_count();
     uint8_t* w = static_cast<uint8_t*>(workspace);
-    cudaError_t e = dsr::launch_decode(*meta, a, qkv, pool->base, out, reinterpret_cast<float*>(w + cb), st,
-                                       meta->n_prefill_tiles > 0, /*fused_append=*/true,
+    cudaError_t e = dsr::launch_decode(*meta, a, qkv, pool->base, out, reinterpret_cast<float*>(w + cb), st, pre,
+                                       /*fused_append=*/true,
                                        merge_in_kernel ? reinterpret_cast<int32_t*>(w) : nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "fused decode kernel");
   }

@@ -88,12 +88,14 @@ enum {
   B_ODONE = 12, B_VLAST = 14, B_DONE = 15, B_VEMPTY = 16, B_COUNT = 18
 };
 
-template <bool BF16, bool HALF, int D, int G>
+template <bool BF16, bool HALF, int D, int G, bool FUSED>
 __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
-    const __grid_constant__ CUtensorMap pool_map, const int4* __restrict__ tiles, int32_t n_atoms,
+    const __grid_constant__ CUtensorMap pool_map, const int4* __restrict__ tiles,
     const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ seq_seen,
-    const int32_t* __restrict__ blk_off, const int32_t* __restrict__ block_table,
-    const uint16_t* __restrict__ qkv, uint16_t* __restrict__ out, LayerArgs a) {
+    const int32_t* __restrict__ seq_new, const int32_t* __restrict__ blk_off,
+    const int32_t* __restrict__ block_table, const int32_t* __restrict__ tok_seq,
+    const int32_t* __restrict__ tok_pos, const uint16_t* __restrict__ qkv, uint16_t* __restrict__ pool,
+    uint16_t* __restrict__ out, LayerArgs a) {
   using C = PfCfg<D>;
   constexpr int T = 128 / G;  // tokens per Q tile
   extern __shared__ uint8_t smem_raw[];
@@ -102,11 +104,67 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * B_COUNT);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int32_t* hdr = a.header;
 
   // Every CTA of this grid stays resident until the prefill work is done, so
   // the decode launch that follows (it needs nothing from this kernel) may
   // start at once on the SMs this grid does not use.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // The batch's atoms and the CTAs that take them (a launch sized by the
+  // capacities has more CTAs; those exit here).
+  const int n_atoms = hdr[HDR_PRE_TILES] * a.Hkv;
+  int n_ctas = hdr[HDR_PRE_CTAS];
+  if (n_ctas <= 0 || n_ctas > (int)gridDim.x) n_ctas = gridDim.x;
+  n_ctas = min(n_ctas, n_atoms);
+  if ((int)blockIdx.x >= n_ctas) return;
+
+  if (FUSED) {
+    // KV append of the prefill chunks' new tokens (decode rows are the decode
+    // kernel's), spread over every working CTA; then a grid barrier, so that
+    // every atom's K/V tiles hold their chunk's new rows before any is loaded.
+    // The launch is cooperative: all n_ctas CTAs are resident, and the wait
+    // is bounded.
+    // One warp per token; a token's units (Hkv * (D/16 + D/8), at most 192)
+    // are spread over the lanes, unrolled so their loads are in flight together.
+    const int N = hdr[HDR_N];
+    constexpr int U = D / 16 + D / 8;
+    const int units = a.Hkv * U;
+    const int n_warps = n_ctas * (C::THREADS / 32);
+    for (int t = blockIdx.x * (C::THREADS / 32) + warp; t < N; t += n_warps) {
+      const int seq = tok_seq[t];
+      if (seq_new[seq] == 1) continue;
+      const int p = tok_pos[t];
+      if (p >= a.max_positions) {
+        if (lane == 0) set_dev_error(hdr, DS_DEVERR_POSITION);
+        continue;
+      }
+      const int blk = block_table[blk_off[seq] + p / kBlockSize];
+      if (blk < 0 || blk >= a.num_blocks) {
+        if (lane == 0) set_dev_error(hdr, DS_DEVERR_BLOCK_ID);
+        continue;
+      }
+      const uint16_t* row = qkv + (int64_t)t * ((a.Hq + 2 * a.Hkv) * D);
+      const float4* cs_row = reinterpret_cast<const float4*>(a.rope + (int64_t)p * (D / 2));
+#pragma unroll 6
+      for (int u = lane; u < units; u += 32) append_unit<BF16, HALF, D>(u, row, cs_row, pool, blk, p % kBlockSize, a);
+    }
+    tc::fence_proxy_async_global();  // this thread's pool writes -> the TMA loads below
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      atomicAdd(&hdr[HDR_PRE_BAR], 1);
+      const long long t0 = clock64();
+      while (*reinterpret_cast<volatile int32_t*>(&hdr[HDR_PRE_BAR]) < n_ctas) {
+        if (clock64() - t0 > DSR_WAIT_LIMIT) {
+          set_dev_error(hdr, DS_DEVERR_WORKLIST);
+          break;
+        }
+      }
+      __threadfence();
+    }
+    __syncthreads();
+  }
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -136,7 +194,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
   // r, r*P + P-1-i for odd r), which evens out the longest-first costs.  Each
   // role walks the same atoms and skips the same malformed ones.
   auto snake_atom = [&](int rnd) -> int {
-    const int P = gridDim.x, i = blockIdx.x;
+    const int P = n_ctas, i = blockIdx.x;
     return rnd * P + ((rnd & 1) ? (P - 1 - i) : i);
   };
   struct Atom {
@@ -491,6 +549,18 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
     tc::fence_before();
     tc::mbar_arrive(&bar[B_DONE]);
   }
+  if (FUSED) {
+    // the last working CTA to finish re-arms the grid barrier for the next
+    // launch on the same upload (every CTA passed it before counting itself)
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      if (atomicAdd(&hdr[HDR_PRE_DONE], 1) == n_ctas - 1) {
+        atomicExch(&hdr[HDR_PRE_BAR], 0);
+        atomicExch(&hdr[HDR_PRE_DONE], 0);
+      }
+    }
+  }
 }
 
 namespace {
@@ -535,58 +605,74 @@ cudaError_t make_pool_map(CUtensorMap* map, const void* pool, const LayerArgs& a
 
 template <bool BF16, bool HALF, int D, int G>
 static cudaError_t launch_prefill_t(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                                    const void* pool, void* out, cudaStream_t st) {
+                                    void* pool, void* out, cudaStream_t st, bool fused) {
   using C = PfCfg<D>;
   CUtensorMap map;
   cudaError_t e = make_pool_map(&map, pool, a);
   if (e != cudaSuccess) return e;
-  auto kern = prefill_tc_kernel<BF16, HALF, D, G>;
+  auto kern = fused ? prefill_tc_kernel<BF16, HALF, D, G, true> : prefill_tc_kernel<BF16, HALF, D, G, false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int n_atoms = m.n_prefill_tiles * a.Hkv;
   // Persistent grid: as many CTAs as SMs, or, with decode rows queued behind
-  // this kernel, the SMs the prefill work needs to finish alongside them.
+  // this kernel, the SMs the prefill work needs to finish alongside them (the
+  // kernel reads the same choice from the header); sized by the SM count
+  // alone when the launch must serve any batch within the capacities.
   int ctas = sms;
-  if (m.prefill_sms > 0.f) ctas = (int)std::ceil(m.prefill_sms);
-  ctas = std::max(1, std::min(ctas, std::min(sms, n_atoms)));
-  kern<<<ctas, C::THREADS, C::SMEM, st>>>(map, reinterpret_cast<const int4*>(m.prefill_tiles), n_atoms,
-                                          m.cu_seqlens, m.seq_seen, m.blk_off, m.block_table,
-                                          static_cast<const uint16_t*>(qkv),
-                                          static_cast<uint16_t*>(out), a);
+  if (!(m.flags & DS_META_CAPACITY)) {
+    const int n_atoms = m.n_prefill_tiles * a.Hkv;
+    if (m.prefill_sms > 0.f) ctas = (int)std::ceil(m.prefill_sms);
+    ctas = std::max(1, std::min(ctas, std::min(sms, n_atoms)));
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // the fused append's grid barrier
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = fused ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, map, reinterpret_cast<const int4*>(m.prefill_tiles), m.cu_seqlens,
+                         m.seq_seen, m.seq_new, m.blk_off, m.block_table, m.tok_seq, m.tok_pos,
+                         static_cast<const uint16_t*>(qkv), static_cast<uint16_t*>(pool),
+                         static_cast<uint16_t*>(out), a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 template <bool BF16, bool HALF, int D>
 static cudaError_t launch_prefill_g(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                                    const void* pool, void* out, cudaStream_t st) {
+                                    void* pool, void* out, cudaStream_t st, bool fu) {
   switch (a.G) {
-    case 1: return launch_prefill_t<BF16, HALF, D, 1>(m, a, qkv, pool, out, st);
-    case 2: return launch_prefill_t<BF16, HALF, D, 2>(m, a, qkv, pool, out, st);
-    case 4: return launch_prefill_t<BF16, HALF, D, 4>(m, a, qkv, pool, out, st);
-    case 8: return launch_prefill_t<BF16, HALF, D, 8>(m, a, qkv, pool, out, st);
+    case 1: return launch_prefill_t<BF16, HALF, D, 1>(m, a, qkv, pool, out, st, fu);
+    case 2: return launch_prefill_t<BF16, HALF, D, 2>(m, a, qkv, pool, out, st, fu);
+    case 4: return launch_prefill_t<BF16, HALF, D, 4>(m, a, qkv, pool, out, st, fu);
+    case 8: return launch_prefill_t<BF16, HALF, D, 8>(m, a, qkv, pool, out, st, fu);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <bool BF16, bool HALF>
 static cudaError_t launch_prefill_d(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                                    const void* pool, void* out, cudaStream_t st) {
-  return a.D == 128 ? launch_prefill_g<BF16, HALF, 128>(m, a, qkv, pool, out, st)
-                    : launch_prefill_g<BF16, HALF, 64>(m, a, qkv, pool, out, st);
+                                    void* pool, void* out, cudaStream_t st, bool fu) {
+  return a.D == 128 ? launch_prefill_g<BF16, HALF, 128>(m, a, qkv, pool, out, st, fu)
+                    : launch_prefill_g<BF16, HALF, 64>(m, a, qkv, pool, out, st, fu);
 }
 
-cudaError_t launch_prefill(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv,
-                           const void* pool, void* out, cudaStream_t st) {
+cudaError_t launch_prefill(const ds_ragged_meta& m, const LayerArgs& a, const void* qkv, void* pool,
+                           void* out, cudaStream_t st, bool fused_append) {
   const bool half = a.style == DS_ROPE_HALF;
+  const bool fu = fused_append;
   if (a.dtype == DS_BF16)
-    return half ? launch_prefill_d<true, true>(m, a, qkv, pool, out, st)
-                : launch_prefill_d<true, false>(m, a, qkv, pool, out, st);
-  return half ? launch_prefill_d<false, true>(m, a, qkv, pool, out, st)
-              : launch_prefill_d<false, false>(m, a, qkv, pool, out, st);
+    return half ? launch_prefill_d<true, true>(m, a, qkv, pool, out, st, fu)
+                : launch_prefill_d<true, false>(m, a, qkv, pool, out, st, fu);
+  return half ? launch_prefill_d<false, true>(m, a, qkv, pool, out, st, fu)
+              : launch_prefill_d<false, false>(m, a, qkv, pool, out, st, fu);
 }
 
 }  // namespace dsr

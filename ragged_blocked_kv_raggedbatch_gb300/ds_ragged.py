@@ -22,6 +22,7 @@ DS_ERR_UNSUPPORTED, DS_ERR_WORKSPACE, DS_ERR_CUDA = 4, 5, 6
 DS_DEVERR_BLOCK_ID, DS_DEVERR_POSITION, DS_DEVERR_WORKLIST, DS_DEVERR_TOKEN = 1, 2, 4, 8
 DS_FP16, DS_BF16 = 0, 1
 DS_ROPE_HALF, DS_ROPE_INTERLEAVED = 0, 1
+DS_META_CAPACITY = 1
 STATUS_NAMES = {0: "DS_OK", 1: "DS_ERR_INVALID_ARG", 2: "DS_ERR_CAPACITY", 3: "DS_ERR_BAD_BLOCK",
                 4: "DS_ERR_UNSUPPORTED", 5: "DS_ERR_WORKSPACE", 6: "DS_ERR_CUDA"}
 
@@ -52,7 +53,7 @@ class ds_rope_table(ctypes.Structure):
 class ds_ragged_meta(ctypes.Structure):
     _fields_ = [("device_buf", P), ("device_bytes", ctypes.c_size_t),
                 ("host_staging", P), ("staging_bytes", ctypes.c_size_t),
-                ("max_seqs", i32), ("max_tokens", i32), ("max_blocks", i32),
+                ("max_seqs", i32), ("max_tokens", i32), ("max_blocks", i32), ("flags", i32),
                 ("n_seqs", i32), ("n_tokens", i32), ("n_blocks", i32),
                 ("n_prefill_seqs", i32), ("n_decode_seqs", i32), ("n_prefill_tiles", i32),
                 ("n_decode_items", i32), ("max_len", i32), ("pool_num_blocks", i32),
@@ -355,7 +356,7 @@ class RaggedLayer:
     torch), plus the three calls of a forward pass."""
 
     def __init__(self, params: ds_attn_params, max_seqs: int, max_tokens: int, max_blocks: int,
-                 max_positions: int, device: str = "cuda", stream=None, workspace=None):
+                 max_positions: int, device: str = "cuda", stream=None, workspace=None, flags: int = 0):
         import torch
         self.params = params
         self.device = device
@@ -364,6 +365,7 @@ class RaggedLayer:
         self.meta_dev = torch.empty(dev_b, dtype=torch.uint8, device=device)
         self.meta_stage = torch.empty(stg_b, dtype=torch.uint8, pin_memory=True)
         self.meta = ds_meta_init(self.meta_dev, self.meta_stage, max_seqs, max_tokens, max_blocks)
+        self.meta.flags = flags
         rb = ds_rope_table_size(params, max_positions)
         self.rope_buf = torch.empty(max(rb, 16), dtype=torch.uint8, device=device)
         self.rope = ds_rope_table_build(params, max_positions, self.rope_buf, stream)
@@ -374,6 +376,12 @@ class RaggedLayer:
 
     def build(self, descs: SeqDescs, pool_num_blocks: int):
         ds_ragged_meta_build(descs, self.params, pool_num_blocks, self.meta, self.stream)
+
+    def pack(self, descs: SeqDescs, pool_num_blocks: int):
+        """Host half of build (validate and pack into the staging buffer; no
+        upload): with DS_META_CAPACITY, what a captured graph's upload then
+        copies for the next replay."""
+        _check(ds_ragged_meta_pack(descs, self.params, pool_num_blocks, self.meta), "ds_ragged_meta_pack")
 
     def append(self, qkv, pool_t, q_out=None):
         pool = ds_kv_pool(pool_t.data_ptr(), pool_t.shape[0])

@@ -102,6 +102,7 @@ int main(int argc, char** argv) {
   CK(ds_meta_buffer_sizes(n_seqs, n_tokens, n_used_blocks, &p, &dev_b, &stg_b));
   ds_ragged_meta meta;
   memset(&meta, 0, sizeof meta);
+  memset(&meta, 0, sizeof meta);
   CU(cudaMalloc(&meta.device_buf, dev_b));
   CU(cudaMallocHost(&meta.host_staging, stg_b));
   meta.device_bytes = dev_b;

@@ -368,3 +368,37 @@ def test_offload_restore_and_gather_validation(lib):
     assert lib.ds_ragged_embedding(R._ref(pk.meta), None, FAKE_DEV, 100, 64, 2, FAKE_DEV, None) == R.DS_ERR_INVALID_ARG
     assert lib.ds_ragged_logits_gather(R._ref(pk.meta), FAKE_DEV, 64, 3, FAKE_DEV, None) == R.DS_ERR_UNSUPPORTED
     assert lib.ds_ragged_logits_gather(None, FAKE_DEV, 64, 2, FAKE_DEV, None) == R.DS_ERR_INVALID_ARG
+
+
+def test_capacity_layout_keeps_every_pointer_and_uploads_the_image(lib):
+    """With DS_META_CAPACITY the regions sit at the offsets the capacities
+    give: two different batches pack to the same device pointers and the same
+    upload size (the whole image), with their counts in the header."""
+    a = W.make_custom([(70, 3), (5, 1), (200, 1)], 8, 2, 128, extra_blocks=20, seed=1)
+    b = W.make_custom([(0, 40), (1000, 1), (64, 64), (9, 1), (300, 1)], 8, 2, 128, extra_blocks=5, seed=2)
+    caps = dict(max_seqs=6, max_tokens=200, max_blocks=40)
+    ptr_names = ["header", "cu_seqlens", "seq_seen", "seq_new", "blk_off", "block_table", "tok_seq", "tok_pos",
+                 "prefill_tiles", "decode_items", "decode_seqs"]
+    got = []
+    for wl in (a, b):
+        pk = Packed(wl, pool_blocks=64, **caps)
+        pk.meta.flags = R.DS_META_CAPACITY
+        assert pk.pack() == R.DS_OK
+        m = pk.meta
+        dev_b, _ = R.ds_meta_buffer_sizes(6, 200, 40, pk.params)
+        assert m.used_bytes <= dev_b and m.used_bytes > dev_b - 256
+        hdr = pk.arrays()["header"]
+        assert list(hdr[[1, 2, 6, 7, 8, 9]]) == [m.n_seqs, m.n_tokens, m.n_prefill_tiles, m.n_decode_items,
+                                                 m.n_decode_seqs, m.split_blocks]
+        assert hdr[10] == int(np.ceil(m.prefill_sms))
+        assert list(hdr[[4, 5, 11, 12]]) == [0, 0, 0, 0]  # the kernels' own counters start at zero
+        ref = oracle.meta_build(wl)
+        arr = pk.arrays()
+        for key in ["cu_seqlens", "seq_seen", "seq_new", "blk_off", "block_table", "tok_seq", "tok_pos"]:
+            np.testing.assert_array_equal(arr[key], ref[key], err_msg=key)
+        got.append([getattr(m, n) for n in ptr_names])
+    assert got[0] == got[1]
+    # without the flag the layout follows each batch's counts
+    pa, pb = Packed(a, pool_blocks=64, **caps), Packed(b, pool_blocks=64, **caps)
+    assert pa.pack() == R.DS_OK and pb.pack() == R.DS_OK
+    assert pa.meta.tok_seq != pb.meta.tok_seq and pa.meta.used_bytes < pb.meta.used_bytes
