@@ -23,7 +23,9 @@
 //   warp 1      tensor-memory owner and MMA issuer (the warp walks the schedule
 //               and builds warp-uniform descriptors; one elected lane issues):
 //                 S_X = Q_X K_t^T   (SS MMA, 128 x 128 x D)
-//                 O_X += P_X V_t    (TS MMA: P read from tensor memory)
+//                 O_X += P_X V_t    (TS MMA: P read from tensor memory, in two
+//                                    halves of 64 keys, each issued as soon as
+//                                    the softmax has written it)
 //               issued as QK_A(0) QK_B(0) | PV_A(t) QK_A(t+1) PV_B(t) QK_B(t+1) ...
 //               so one tile's softmax overlaps the other tile's MMAs.
 //   warps 2-3   no work (they only return their registers)
@@ -53,6 +55,15 @@
 #define DSR_PF_REG_HIGH 200
 #endif
 static_assert(128 * DSR_PF_REG_LOW + 256 * DSR_PF_REG_HIGH <= 384 * 168, "register split over the launch budget");
+// Atom order.  0: atom k is (tile k / Hkv, KV head k % Hkv): the atoms running
+// at once cover every head.  1: (head k / tiles, tile k % tiles): they read
+// one head's K/V prefixes, which stay in L2 for the atoms that follow.
+// Measured on GB300 (attention call), 0 -> 1: chunked prefill 2x8192 2.682 ->
+// 2.866 ms although its DRAM traffic drops from 1.47x to 1.02x the
+// algorithmic bytes; max ragged batch, seed 1: 0.787 -> 0.935 ms.
+#ifndef DSR_PF_HEAD_MAJOR
+#define DSR_PF_HEAD_MAJOR 0
+#endif
 // 1: K/V tile loads carry an L2 evict_last policy (every atom of a chunk re-reads
 // its sequence's K/V prefix from L2).
 #ifndef DSR_PF_EVICT_LAST
@@ -83,10 +94,15 @@ struct PfCfg {
 // K and V slots of a ring stage are released separately: K once the last
 // QK MMA of its step has read it, V once the last PV MMA has, so the next K
 // tile is requested a whole step before it is needed.
+// P is handed to the P*V MMAs in two halves of 64 keys (B_PFULL + 2x + half):
+// the first four K-steps of P*V start while the softmax still computes the
+// second half.  B_ODONE0 + x: the first half of P*V(x) is done (its P columns
+// may be overwritten).
 enum {
   B_QREADY = 0, B_KFULL = 2, B_VFULL = 4, B_KEMPTY = 6, B_SFULL = 8, B_PFULL = 10,
-  B_ODONE = 12, B_VLAST = 14, B_DONE = 15, B_VEMPTY = 16, B_COUNT = 18
+  B_ODONE = 14, B_ODONE0 = 16, B_VLAST = 18, B_DONE = 19, B_VEMPTY = 20, B_COUNT = 22
 };
+static_assert(8 * B_COUNT + 4 <= 256, "barriers and the tensor-memory slot fit the reserved bytes");
 
 template <bool BF16, bool HALF, int D, int G, bool FUSED>
 __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
@@ -174,8 +190,10 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
       mbar_init(&bar[B_KEMPTY + s], 1);
       mbar_init(&bar[B_VEMPTY + s], 1);
       mbar_init(&bar[B_SFULL + s], 1);
-      mbar_init(&bar[B_PFULL + s], 128);
+      mbar_init(&bar[B_PFULL + 2 * s], 128);
+      mbar_init(&bar[B_PFULL + 2 * s + 1], 128);
       mbar_init(&bar[B_ODONE + s], 1);
+      mbar_init(&bar[B_ODONE0 + s], 1);
     }
     mbar_init(&bar[B_VLAST], 1);
     mbar_init(&bar[B_DONE], 256);
@@ -189,7 +207,8 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
   uint8_t* sQ = sm + C::OFF_Q;
   uint8_t* sKV = sm + C::OFF_KV;
 
-  // Atom k of the work list: prefill tile k / Hkv (longest first), KV head k % Hkv.
+  // Atom k of the work list: one (prefill tile, KV head) pair, tiles longest
+  // first (DSR_PF_HEAD_MAJOR sets the order of the pairs).
   // CTA i takes one atom per round in snake order (round r: r*P + i for even
   // r, r*P + P-1-i for odd r), which evens out the longest-first costs.  Each
   // role walks the same atoms and skips the same malformed ones.
@@ -202,10 +221,16 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
     bool has_b;
     const int* btab;
   };
+  const int n_tiles = hdr[HDR_PRE_TILES];
   auto load_atom = [&](int k, Atom& at) -> bool {
+#if DSR_PF_HEAD_MAJOR
+    const int4 tl = tiles[k % n_tiles];
+    at.c = k / n_tiles;
+#else
     const int4 tl = tiles[k / a.Hkv];
-    at.seq = tl.x; at.j0 = tl.y; at.ntok = tl.z; at.kv_len = tl.w;
     at.c = k % a.Hkv;
+#endif
+    at.seq = tl.x; at.j0 = tl.y; at.ntok = tl.z; at.kv_len = tl.w;
     at.s_seen = seq_seen[at.seq];
     at.tok0 = cu_seqlens[at.seq] + at.j0;
     at.btab = block_table + blk_off[at.seq];
@@ -334,17 +359,25 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
           }
           __syncwarp();
         };
-        auto pv = [&](int x, uint32_t r, bool acc) {
+        // O_x += P_x V_t in two halves of 64 keys, each issued once the
+        // softmax has written that half of P
+        auto pv = [&](int x, uint32_t r, bool acc, uint32_t parity) -> bool {
           const uint64_t vd =
               tc::smem_desc_sw128(smem_u32(sKV + (r & 1) * 2 * C::KVTILE + C::KVTILE), C::KHALF, 1024);
-          if (tc::elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              tc::mma_ts(tmem + C::COL_O0 + D * x, tmem + C::COL_S0 + 128 * x + 8 * kk,
-                         vd + ((kk * 2048) >> 4), IPV, (acc || kk > 0));
-            tc::mma_commit(&bar[B_ODONE + x]);
+          for (int half = 0; half < 2; ++half) {
+            if (!wait(B_PFULL + 2 * x + half, parity)) return false;
+            tc::fence_after();
+            if (tc::elect_one()) {
+#pragma unroll
+              for (int kk = 4 * half; kk < 4 * half + 4; ++kk)
+                tc::mma_ts(tmem + C::COL_O0 + D * x, tmem + C::COL_S0 + 128 * x + 8 * kk,
+                           vd + ((kk * 2048) >> 4), IPV, (acc || kk > 0));
+              tc::mma_commit(&bar[(half ? B_ODONE : B_ODONE0) + x]);
+            }
+            __syncwarp();
           }
-          __syncwarp();
+          return true;
         };
         uint32_t ring = 0, qn[2] = {0, 0}, stp[2] = {0, 0};
         bool ok = true;
@@ -366,10 +399,8 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
           commit(B_KEMPTY + (ring & 1));
           for (int t = 0; t < at.n_kv; ++t) {
             const uint32_t r = ring + t;
-            ok = wait(B_VFULL + (r & 1), (r >> 1) & 1) && wait(B_PFULL + 0, stp[0] & 1);
+            ok = wait(B_VFULL + (r & 1), (r >> 1) & 1) && pv(0, r, t > 0, stp[0] & 1);
             if (!ok) break;
-            tc::fence_after();
-            pv(0, r, t > 0);
             ++stp[0];
             if (t + 1 < at.n_kv) {
               ok = wait(B_KFULL + ((r + 1) & 1), ((r + 1) >> 1) & 1);
@@ -378,10 +409,8 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
               qk(0, r + 1);
             }
             if (at.has_b) {
-              ok = wait(B_PFULL + 1, stp[1] & 1);
+              ok = pv(1, r, t > 0, stp[1] & 1);
               if (!ok) break;
-              tc::fence_after();
-              pv(1, r, t > 0);
               ++stp[1];
             }
             commit(B_VEMPTY + (r & 1));
@@ -484,43 +513,55 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
           alpha = fast_exp2(m_ref - mx);
           m_ref = mx;
         }
-        if (t > 0) {  // P(t) overwrites P(t-1); O must hold PV(t-1) before a rescale
+        // tensor-memory loads/stores are warp-collective: rescale O as a warp
+        // whenever any of its rows needs it (alpha = 1 for the others), before
+        // any P*V(t) accumulates into it; that needs P*V(t-1) complete
+        const bool resc = t > 0 && __any_sync(0xffffffffu, mine);
+        if (resc) {
           if (!mbar_wait_bounded(&bar[B_ODONE + x], (stp - 1) & 1)) { ok = false; break; }
           tc::fence_after();
+          // 16 columns at a time: the 128 scores of the row are still live
+#pragma unroll 1
+          for (int ch = 0; ch < D / 16; ++ch) {
+            uint32_t o[16];
+            tc::tmem_ld16(lane_addr + col_o + 16 * ch, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tc::tmem_st16(lane_addr + col_o + 16 * ch, o);
+          }
         }
         const float nm = -m_ref;
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float y0, y1;
-            tc::ffma2(y0, y1, __uint_as_float(v[32 * ch + 2 * e]), __uint_as_float(v[32 * ch + 2 * e + 1]),
-                      sc, sc, nm, nm);
-            const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
-            tc::fadd2(s0, s1, p0, p1);
-            pk[e] = Stor<BF16>::pack(p0, p1);
+        for (int half = 0; half < 2; ++half) {
+          // P(t) overwrites P(t-1): that half of P*V(t-1) must be done
+          if (t > 0 && !resc &&
+              !mbar_wait_bounded(&bar[(half ? B_ODONE : B_ODONE0) + x], (stp - 1) & 1)) {
+            ok = false;
+            break;
           }
-          tc::tmem_st16(lane_addr + col_s + 16 * ch, pk);
+          tc::fence_after();
+#pragma unroll
+          for (int ch = 2 * half; ch < 2 * half + 2; ++ch) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              float y0, y1;
+              tc::ffma2(y0, y1, __uint_as_float(v[32 * ch + 2 * e]), __uint_as_float(v[32 * ch + 2 * e + 1]),
+                        sc, sc, nm, nm);
+              const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+              tc::fadd2(s0, s1, p0, p1);
+              pk[e] = Stor<BF16>::pack(p0, p1);
+            }
+            tc::tmem_st16(lane_addr + col_s + 16 * ch, pk);
+          }
+          tc::tmem_wait_st();
+          tc::fence_before();
+          tc::mbar_arrive(&bar[B_PFULL + 2 * x + half]);
         }
+        if (!ok) break;
         l = l * alpha + (s0 + s1);
-        // tensor-memory loads/stores are warp-collective: rescale O as a warp
-        // whenever any of its rows needs it (alpha = 1 for the others)
-        if (t > 0 && __any_sync(0xffffffffu, mine)) {
-#pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t o[32];
-            tc::tmem_ld32(lane_addr + col_o + 32 * ch, o);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tc::tmem_st32(lane_addr + col_o + 32 * ch, o);
-          }
-        }
-        tc::tmem_wait_st();
-        tc::fence_before();
-        tc::mbar_arrive(&bar[B_PFULL + x]);
       }
       if (!ok) break;
       // epilogue: the atom's last P*V, then O / l -> out
