@@ -29,7 +29,8 @@ enum : int {
   HDR_SPLIT = 9,      // KV blocks per decode split
   HDR_PRE_CTAS = 10,  // CTAs of the prefill grid that work (0: one per SM)
   HDR_PRE_BAR = 11,   // fused prefill: CTAs past the append prologue
-  HDR_PRE_DONE = 12,  // fused prefill: CTAs finished; the last one zeroes 11, 12
+  HDR_PRE_DONE = 12,  // prefill CTAs finished; the last one zeroes 11, 12, 13
+  HDR_PRE_NEXT = 13,  // prefill atoms handed out so far
   HDR_WORDS = 16,
 };
 

@@ -326,14 +326,26 @@ ds_status ds_ragged_meta_pack(const ds_seq_desc* seqs, int32_t n_seqs,
     tiles[4 * k + 2] = tv[k].ntok;
     tiles[4 * k + 3] = tv[k].kv_len;
   }
-  // Decode split items and per-decode-sequence item ranges.  A sequence with a
-  // single item writes its output directly (partial slot -1).
+  // Decode split items and per-decode-sequence item ranges, the longest rows
+  // first: the tensor-core decode kernel takes its units in this order, so
+  // the last units taken are the short ones (in batch order, a 32-block unit
+  // taken last left a ~60 us tail on the max ragged batch).  A row's items
+  // stay consecutive; a row with a single item writes its output directly
+  // (partial slot -1).
+  thread_local std::vector<std::pair<int32_t, int32_t>> dec_rows;  // (blocks, sequence)
+  dec_rows.clear();
+  for (int32_t i = 0; i < n_seqs; ++i)
+    if (seqs[i].new_tokens == 1)
+      dec_rows.push_back({(int32_t)(((int64_t)seqs[i].seen_tokens + 1 + bs - 1) / bs), i});
+  std::stable_sort(dec_rows.begin(), dec_rows.end(),
+                   [](const std::pair<int32_t, int32_t>& a, const std::pair<int32_t, int32_t>& b) {
+                     return a.first > b.first;
+                   });
   int64_t it = 0;
   int32_t di = 0;
-  for (int32_t i = 0; i < n_seqs; ++i) {
-    const ds_seq_desc& d = seqs[i];
-    if (d.new_tokens != 1) continue;
-    int32_t nb = (int32_t)(((int64_t)d.seen_tokens + 1 + bs - 1) / bs);
+  for (const auto& row : dec_rows) {
+    const int32_t i = row.second;
+    const int32_t nb = row.first;
     int32_t cnt = (nb + split - 1) / split;
     dseqs[4 * di + 0] = i;
     dseqs[4 * di + 1] = cu[i];

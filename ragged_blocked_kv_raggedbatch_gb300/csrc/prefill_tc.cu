@@ -7,14 +7,18 @@
 // per head size): up to 256/G consecutive new tokens of one sequence and one
 // KV head c, as two Q tiles of 128 rows (tokens x the G query heads that read
 // KV head c).  Both tiles share every 128-key K/V tile, which is two 64-token
-// pool blocks fetched through the block table.  The grid is persistent: CTA i
-// takes one atom per round of the longest-first list (snake order); the K/V ring,
-// barrier phases and tensor memory carry over from one atom to the next.
+// pool blocks fetched through the block table.  The grid is persistent: each
+// CTA takes the next atom of the longest-first list when it is ready for one;
+// the K/V ring, barrier phases and tensor memory carry over from one atom to
+// the next.
 //
 // Roles (12 warps = 3 warpgroups; launched at 168 registers a thread, the
 // first warpgroup gives registers back (setmaxnreg 96) and the two softmax
 // warpgroups take them (setmaxnreg 200): 128*96 + 2*128*200 <= 384*168):
-//   warp 0      TMA producer: K and V tiles into 2-stage rings whose slots are
+//   warp 0      takes the atoms (longest first, from a counter in the batch
+//               header, one as the previous one's last tile is issued) and
+//               hands them to the others; TMA producer: K and V tiles into
+//               2-stage rings whose slots are
 //               freed separately (K after the last QK MMA that reads it, V after
 //               the last PV MMA), so each K tile is requested about a step and a
 //               half before its first QK; zeroes the rows of the final V tile
@@ -85,7 +89,7 @@ struct PfCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = 2 * QTILE;
   static constexpr int OFF_BAR = OFF_KV + 2 * 2 * KVTILE;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;
   static constexpr int COL_S0 = 0, COL_O0 = 256;
   static constexpr int TMEM_COLS = 512;
   static constexpr int THREADS = 384;
@@ -98,11 +102,16 @@ struct PfCfg {
 // the first four K-steps of P*V start while the softmax still computes the
 // second half.  B_ODONE0 + x: the first half of P*V(x) is done (its P columns
 // may be overwritten).
+// B_AFULL / B_AEMPTY: the atom ring (AQ slots) the scheduler warp fills.
+constexpr int AQ = 4;
 enum {
   B_QREADY = 0, B_KFULL = 2, B_VFULL = 4, B_KEMPTY = 6, B_SFULL = 8, B_PFULL = 10,
-  B_ODONE = 14, B_ODONE0 = 16, B_VLAST = 18, B_DONE = 19, B_VEMPTY = 20, B_COUNT = 22
+  B_ODONE = 14, B_ODONE0 = 16, B_VLAST = 18, B_DONE = 19, B_VEMPTY = 20, B_AFULL = 22,
+  B_AEMPTY = B_AFULL + AQ, B_COUNT = B_AEMPTY + AQ
 };
-static_assert(8 * B_COUNT + 4 <= 256, "barriers and the tensor-memory slot fit the reserved bytes");
+// arrivals that free an atom slot: the MMA warp, 8 softmax warps
+constexpr int AEMPTY_ARRIVALS = 9;
+static_assert(8 * B_COUNT + 4 + 4 * AQ <= 512, "barriers, tensor-memory slot and atom ring fit the reserved bytes");
 
 template <bool BF16, bool HALF, int D, int G, bool FUSED>
 __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
@@ -119,6 +128,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
   uint8_t* sm = smem_raw + (((raw_u + 1023u) & ~1023u) - raw_u);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * B_COUNT);
+  int* aring = reinterpret_cast<int*>(sm + C::OFF_BAR + 8 * B_COUNT + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int32_t* hdr = a.header;
 
@@ -196,6 +206,10 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
       mbar_init(&bar[B_ODONE0 + s], 1);
     }
     mbar_init(&bar[B_VLAST], 1);
+    for (int q = 0; q < AQ; ++q) {
+      mbar_init(&bar[B_AFULL + q], 1);
+      mbar_init(&bar[B_AEMPTY + q], AEMPTY_ARRIVALS);
+    }
     mbar_init(&bar[B_DONE], 256);
     fence_barrier_init();
   }
@@ -208,13 +222,26 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
   uint8_t* sKV = sm + C::OFF_KV;
 
   // Atom k of the work list: one (prefill tile, KV head) pair, tiles longest
-  // first (DSR_PF_HEAD_MAJOR sets the order of the pairs).
-  // CTA i takes one atom per round in snake order (round r: r*P + i for even
-  // r, r*P + P-1-i for odd r), which evens out the longest-first costs.  Each
-  // role walks the same atoms and skips the same malformed ones.
-  auto snake_atom = [&](int rnd) -> int {
-    const int P = n_ctas, i = blockIdx.x;
-    return rnd * P + ((rnd & 1) ? (P - 1 - i) : i);
+  // first (DSR_PF_HEAD_MAJOR sets the order of the pairs).  Each role walks
+  // the same atoms and skips the same malformed ones.
+  // Atoms are taken dynamically, longest first: the TMA producer takes the
+  // next index from a counter in the batch header when it has issued the
+  // last K/V tile of its current atom (so a CTA holds at most about two KV
+  // steps of look-ahead), and publishes it in a ring of AQ slots that the
+  // MMA and softmax warps read in order (so all walk the same atoms).  A
+  // static assignment left a 120 us straggler on the max ragged batch, whose
+  // atoms span 32 to 24,872 keys; a scheduler warp filling the ring ahead let
+  // one CTA take several of the longest atoms at once.  next_atom returns -1
+  // when the atoms are exhausted or a wait ran out (then ok = false).
+  auto next_atom = [&](uint32_t& i, bool& ok) -> int {
+    const int q = i % AQ;
+    const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&bar[B_AFULL + q], (i / AQ) & 1));
+    const int k = got ? aring[q] : -1;
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&bar[B_AEMPTY + q]);
+    ++i;
+    if (!got) ok = false;
+    return k;
   };
   struct Atom {
     int seq, j0, ntok, kv_len, c, s_seen, tok0, n_kv;
@@ -260,7 +287,22 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
 #define DSR_PF_TMA(dst, c0, c1, b) tc::tma_load_2d(dst, &pool_map, c0, c1, b)
 #endif
       bool ok = true;
-      for (int rnd = 0, k = snake_atom(0); ok && k < n_atoms; k = snake_atom(++rnd)) {
+      for (uint32_t ai = 0; ok; ++ai) {
+        // take the next atom and hand it to the MMA and softmax warps
+        const int q = ai % AQ;
+        if (ai >= AQ && !__all_sync(0xffffffffu, mbar_wait_bounded(&bar[B_AEMPTY + q], ((ai / AQ) - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        int k = 0;
+        if (lane == 0) k = atomicAdd(&hdr[HDR_PRE_NEXT], 1);
+        k = __shfl_sync(0xffffffffu, k, 0);
+        if (k >= n_atoms) k = -1;
+        if (lane == 0) {
+          aring[q] = k;
+          tc::mbar_arrive(&bar[B_AFULL + q]);
+        }
+        if (k < 0) break;
         Atom at;
         if (!load_atom(k, at)) continue;
         for (int t = 0; t < at.n_kv; ++t, ++ring) {
@@ -381,7 +423,9 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
         };
         uint32_t ring = 0, qn[2] = {0, 0}, stp[2] = {0, 0};
         bool ok = true;
-        for (int rnd = 0, k = snake_atom(0); ok && k < n_atoms; k = snake_atom(++rnd)) {
+        for (uint32_t ai = 0; ok;) {
+          const int k = next_atom(ai, ok);
+          if (k < 0) break;
           Atom at;
           if (!load_atom(k, at)) continue;
           ok = wait(B_QREADY + 0, qn[0] & 1) && wait(B_KFULL + (ring & 1), (ring >> 1) & 1);
@@ -442,7 +486,9 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
     const float sc = a.scale_log2;
     uint32_t stp = 0;  // KV steps of tile x done by this CTA
     bool ok = true;
-    for (int rnd = 0, k = snake_atom(0); ok && k < n_atoms; k = snake_atom(++rnd)) {
+    for (uint32_t ai = 0; ok;) {
+      const int k = next_atom(ai, ok);
+      if (k < 0) break;
       Atom at;
       if (!load_atom(k, at)) continue;
       if (x == 1 && !at.has_b) continue;
@@ -590,16 +636,16 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
     tc::fence_before();
     tc::mbar_arrive(&bar[B_DONE]);
   }
-  if (FUSED) {
-    // the last working CTA to finish re-arms the grid barrier for the next
-    // launch on the same upload (every CTA passed it before counting itself)
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      if (atomicAdd(&hdr[HDR_PRE_DONE], 1) == n_ctas - 1) {
-        atomicExch(&hdr[HDR_PRE_BAR], 0);
-        atomicExch(&hdr[HDR_PRE_DONE], 0);
-      }
+  // the last working CTA to finish re-arms the atom counter (and the fused
+  // variant's grid barrier) for the next launch on the same upload: every CTA
+  // took its last atom (and passed the barrier) before counting itself
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(&hdr[HDR_PRE_DONE], 1) == n_ctas - 1) {
+      atomicExch(&hdr[HDR_PRE_NEXT], 0);
+      atomicExch(&hdr[HDR_PRE_BAR], 0);
+      atomicExch(&hdr[HDR_PRE_DONE], 0);
     }
   }
 }

@@ -148,9 +148,13 @@ def _check_coverage(wl, meta, got):
     assert sum(cover.values()) == int(wl.new[wl.new > 1].sum())
     dec = [i for i in range(wl.n_seqs) if wl.new[i] == 1]
     assert len(got["decode_seqs"]) == len(dec)
+    # every decode row once, the longest first (ties in batch order)
+    order = [int(r[0]) for r in got["decode_seqs"]]
+    assert sorted(order) == dec
+    assert order == sorted(dec, key=lambda i: -(-(-(int(wl.seen[i]) + 1) // 64)))
     slots = []
     for k, (seq, tok, first, cnt) in enumerate(got["decode_seqs"]):
-        assert seq == dec[k] and tok == got["cu_seqlens"][seq]
+        assert tok == got["cu_seqlens"][seq]
         nb = -(-(int(wl.seen[seq]) + 1) // 64)
         blocks = []
         split = meta.split_blocks
