@@ -51,15 +51,15 @@ SINGLE_THREAD_ORACLE = ("tiny_gqa_d64", "decode256_mha_d128", "splitfuse2048_gqa
 # removed) still matches the capture.
 NCU_TRAFFIC = {
     # decode_split_kernel on the first 64 sequences of the decode-only batch:
-    # 2.290088 GB read + 5.80 MB written for 2.2576 GB algorithmic (x1.0170);
+    # 2.290063 GB read + 6.02 MB written for 2.2576 GB algorithmic (x1.0171);
     # scaled to the full batch by its algorithmic bytes (the KV read dominates
     # and grows in proportion).
-    "decode256_mha_d128": {"bytes": 9.377e9, "files": ["decode.cu", "common.cuh", "tc.cuh"],
-                           "src": "6f868d52f8c764c0"},
+    "decode256_mha_d128": {"bytes": 9.3776e9, "files": ["decode.cu", "common.cuh", "tc.cuh"],
+                           "src": "69acc4e8a58215d6"},
     # prefill_tc_kernel on the whole chunked-prefill workload (< 1 GB on the
-    # device, captured at full size): 714.54 MB read + 224.78 MB written.
-    "chunked_prefill_2x8192": {"bytes": 9.39321e8, "files": ["prefill_tc.cu", "common.cuh", "tc.cuh"],
-                               "src": "dcb73b12bc171f53"},
+    # device, captured at full size): 723.16 MB read + 226.79 MB written.
+    "chunked_prefill_2x8192": {"bytes": 9.49953e8, "files": ["prefill_tc.cu", "common.cuh", "tc.cuh"],
+                               "src": "76453887da724dc8"},
 }
 
 
