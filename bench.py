@@ -407,11 +407,11 @@ def device_measure(wl, args, grp, local, K, warmup, keep=False, flushed_loop=Tru
     fused = args.path == "fused"
     if fused:
         # prefill tiles (their K/V append inside), decode rows (append + split-K,
-        # the merge inside on the tensor-core path, or while the CUDA-core
-        # kernel's grid is at most two waves)
+        # the merge inside on the tensor-core path, beside a prefill grid, or
+        # while the CUDA-core kernel's grid is at most two waves)
         sms = torch.cuda.get_device_properties(local).multi_processor_count
         tc_decode = wl.head_dim == 128 and wl.n_q_heads // wl.n_kv_heads >= 2
-        merge_inside = tc_decode or m.n_decode_items * wl.n_kv_heads <= 6 * sms
+        merge_inside = tc_decode or m.n_prefill_tiles > 0 or m.n_decode_items * wl.n_kv_heads <= 6 * sms
         launches_per_step = (m.n_prefill_tiles > 0) + (m.n_decode_items > 0) + \
             (not merge_inside and m.n_decode_items > m.n_decode_seqs)
     else:

@@ -263,21 +263,23 @@ ds_status ds_blocked_attention(const ds_ragged_meta* meta, const ds_attn_params*
  * allows.  This is operator fusion as "Principle: Deepspeedai DeepSpeed Inference Engine
  * Init" (leeroopedia), section "Theoretical Basis", describes it: fewer, larger
  * kernels cut launch overhead and the round trip of intermediates.  The
- * RoPE-and-append of a decode row happens inside the attention kernel that
- * reads the row's KV.
+ * RoPE-and-append of each new token happens inside an attention kernel, so a
+ * call is at most two launches and no separate append kernel runs.
  *
  * Results: exactly those of ds_kv_rotary_append(meta, params, rope, qkv, NULL,
  * pool) followed by ds_blocked_attention on the same stream: the same pool
  * contents and the same output bits.
  * Launches:
- *  - decode rows: the split-K kernel appends each row's new K/V in the split
- *    that holds its last block.  While its grid is at most two waves
- *    (n_decode_items * n_kv_heads <= 6 * SMs) the last split of each (row, KV
- *    head) also merges the partials, so a decode-only batch is 1 launch.
- *    Larger grids merge in a separate kernel (2 launches), which costs less
- *    there.
- *  - prefill tiles: the append kernel over prefill tokens only, then the
- *    prefill kernel; decode rows follow as above.
+ *  - prefill tiles: the prefill kernel, launched cooperatively, first appends
+ *    the prefill chunks' new K/V (a prologue over all its CTAs), meets at a
+ *    grid barrier, then computes its tiles.
+ *  - decode rows: the decode kernel appends each row's new K/V in the split
+ *    that holds the row's last KV block, before that block is read, and merges
+ *    the split partials of each (row, KV head) in the CTA that finishes last.
+ *    Only a decode-only batch on the CUDA-core kernel with a grid above two
+ *    waves (n_decode_items * n_kv_heads > 6 * SMs) merges in a separate
+ *    kernel instead, which costs less there.
+ *  So a batch is 1 launch (prefill only, or decode only) or 2.
  *
  * Workspace: DEVICE, 256-byte aligned, ws_bytes >= ds_fused_workspace_size for
  * the meta object's capacities.  It starts with one int32 counter per

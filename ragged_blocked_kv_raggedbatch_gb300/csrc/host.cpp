@@ -606,12 +606,13 @@ ds_status ds_fused_append_attention(const ds_ragged_meta* meta, const ds_attn_pa
   if (cap || meta->n_decode_items > 0) {
     // Decode rows append their own K/V.  Their split partials are merged
     // inside the decode kernel by the tensor-core kernel, and by the CUDA-core
-    // one while its grid is at most two waves of 3 CTAs per SM (on a larger
-    // grid the separate merge launch costs less than holding every CTA for its
+    // one whenever a prefill grid runs too (so a call is at most two launches),
+    // its grid is at most two waves of 3 CTAs per SM, or the launch must serve
+    // any batch within the capacities.  A larger decode-only grid keeps the
+    // separate merge launch, which costs less than holding every CTA for its
     // count: decode-only batch of 256 rows on GB300, 1.304 ms merged in the
-    // kernel against 1.297 ms with the merge kernel), and always in a launch
-    // that must serve any batch within the capacities.
-    const bool merge_in_kernel = cap || dsr::decode_on_tensor_cores(a) ||
+    // kernel against 1.297 ms with the merge kernel.
+    const bool merge_in_kernel = cap || pre || dsr::decode_on_tensor_cores(a) ||
                                  (int64_t)meta->n_decode_items * params->n_kv_heads <= 6LL * device_sm_count();
     uint8_t* w = static_cast<uint8_t*>(workspace);
     cudaError_t e = dsr::launch_decode(*meta, a, qkv, pool->base, out, reinterpret_cast<float*>(w + cb), st, pre,
