@@ -57,9 +57,10 @@ NCU_TRAFFIC = {
     "decode256_mha_d128": {"bytes": 9.3776e9, "files": ["decode.cu", "common.cuh", "tc.cuh"],
                            "src": "69acc4e8a58215d6"},
     # prefill_tc_kernel on the whole chunked-prefill workload (< 1 GB on the
-    # device, captured at full size): 723.16 MB read + 226.79 MB written.
-    "chunked_prefill_2x8192": {"bytes": 9.49953e8, "files": ["prefill_tc.cu", "common.cuh", "tc.cuh"],
-                               "src": "76453887da724dc8"},
+    # device, captured at full size): 459.60 MB read + 226.74 MB written for
+    # 637.5 MB algorithmic (x1.077).
+    "chunked_prefill_2x8192": {"bytes": 6.86337e8, "files": ["prefill_tc.cu", "common.cuh", "tc.cuh"],
+                               "src": "7aee36208be0d9b6"},
 }
 
 

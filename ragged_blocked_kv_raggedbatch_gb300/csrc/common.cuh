@@ -31,6 +31,7 @@ enum : int {
   HDR_PRE_BAR = 11,   // fused prefill: CTAs past the append prologue
   HDR_PRE_DONE = 12,  // prefill CTAs finished; the last one zeroes 11, 12, 13
   HDR_PRE_NEXT = 13,  // prefill atoms handed out so far
+  HDR_PRE_HG = 14,    // KV heads per group in the prefill atom order (0: all)
   HDR_WORDS = 16,
 };
 

@@ -59,15 +59,6 @@
 #define DSR_PF_REG_HIGH 200
 #endif
 static_assert(128 * DSR_PF_REG_LOW + 256 * DSR_PF_REG_HIGH <= 384 * 168, "register split over the launch budget");
-// Atom order.  0: atom k is (tile k / Hkv, KV head k % Hkv): the atoms running
-// at once cover every head.  1: (head k / tiles, tile k % tiles): they read
-// one head's K/V prefixes, which stay in L2 for the atoms that follow.
-// Measured on GB300 (attention call), 0 -> 1: chunked prefill 2x8192 2.682 ->
-// 2.866 ms although its DRAM traffic drops from 1.47x to 1.02x the
-// algorithmic bytes; max ragged batch, seed 1: 0.787 -> 0.935 ms.
-#ifndef DSR_PF_HEAD_MAJOR
-#define DSR_PF_HEAD_MAJOR 0
-#endif
 // 1: K/V tile loads carry an L2 evict_last policy (every atom of a chunk re-reads
 // its sequence's K/V prefix from L2).
 #ifndef DSR_PF_EVICT_LAST
@@ -200,8 +191,8 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
       mbar_init(&bar[B_KEMPTY + s], 1);
       mbar_init(&bar[B_VEMPTY + s], 1);
       mbar_init(&bar[B_SFULL + s], 1);
-      mbar_init(&bar[B_PFULL + 2 * s], 128);
-      mbar_init(&bar[B_PFULL + 2 * s + 1], 128);
+      mbar_init(&bar[B_PFULL + 2 * s], 4);  // one arrival per softmax warp
+      mbar_init(&bar[B_PFULL + 2 * s + 1], 4);
       mbar_init(&bar[B_ODONE + s], 1);
       mbar_init(&bar[B_ODONE0 + s], 1);
     }
@@ -222,7 +213,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
   uint8_t* sKV = sm + C::OFF_KV;
 
   // Atom k of the work list: one (prefill tile, KV head) pair, tiles longest
-  // first (DSR_PF_HEAD_MAJOR sets the order of the pairs).  Each role walks
+  // first, KV heads in groups (see below).  Each role walks
   // the same atoms and skips the same malformed ones.
   // Atoms are taken dynamically, longest first: the TMA producer takes the
   // next index from a counter in the batch header when it has issued the
@@ -250,13 +241,21 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
   };
   const int n_tiles = hdr[HDR_PRE_TILES];
   auto load_atom = [&](int k, Atom& at) -> bool {
-#if DSR_PF_HEAD_MAJOR
-    const int4 tl = tiles[k % n_tiles];
-    at.c = k / n_tiles;
-#else
-    const int4 tl = tiles[k / a.Hkv];
-    at.c = k % a.Hkv;
-#endif
+    // Tiles longest first in rounds of R = n_ctas / hg tiles; within a
+    // round, the KV heads in groups of hg (the batch header's choice), each
+    // group's atoms tile-major.  hg = all heads is plain tile-major order:
+    // the atoms running at once then read every head's K/V prefix; with a
+    // smaller hg they read those of hg heads, which L2 holds more easily.
+    int hg = hdr[HDR_PRE_HG];
+    if (hg <= 0 || hg > a.Hkv || a.Hkv % hg != 0) hg = a.Hkv;
+    const int R = max(1, n_ctas / hg);        // tiles per round
+    const int round = k / (R * a.Hkv);
+    const int t0 = round * R;                 // first tile of the round
+    const int rt = min(R, n_tiles - t0);      // tiles in the round
+    const int j = k - round * R * a.Hkv;      // atom within the round, < rt * Hkv
+    const int jj = j % (rt * hg);
+    const int4 tl = tiles[t0 + jj / hg];
+    at.c = (j / (rt * hg)) * hg + jj % hg;
     at.seq = tl.x; at.j0 = tl.y; at.ntok = tl.z; at.kv_len = tl.w;
     at.s_seen = seq_seen[at.seq];
     at.tok0 = cu_seqlens[at.seq] + at.j0;
@@ -604,7 +603,8 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
           }
           tc::tmem_wait_st();
           tc::fence_before();
-          tc::mbar_arrive(&bar[B_PFULL + 2 * x + half]);
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&bar[B_PFULL + 2 * x + half]);
         }
         if (!ok) break;
         l = l * alpha + (s0 + s1);

@@ -406,3 +406,21 @@ def test_capacity_layout_keeps_every_pointer_and_uploads_the_image(lib):
     pa, pb = Packed(a, pool_blocks=64, **caps), Packed(b, pool_blocks=64, **caps)
     assert pa.pack() == R.DS_OK and pb.pack() == R.DS_OK
     assert pa.meta.tok_seq != pb.meta.tok_seq and pa.meta.used_bytes < pb.meta.used_bytes
+
+
+def test_prefill_head_group_follows_the_longest_atom(lib):
+    """Header word 14 orders the prefill atoms: one KV head at a time when the
+    longest atom is short against a CTA's share of the prefill work (the
+    chunked prefill), two otherwise, all heads (tile-major) when one atom
+    outlasts that share; 0 when there is no prefill tile."""
+    cases = [(W.make_workload("chunked_prefill_2x8192", 0), 1),
+             (W.make_workload("max_ragged_8192", 0), 1),
+             (W.make_workload("max_ragged_8192", 2), 2),
+             (W.make_workload("tiny_gqa_d64", 0), 0),
+             (W.make_workload("decode256_mha_d128", 0), 0)]
+    for wl, want in cases:
+        pk = Packed(wl)
+        assert pk.pack() == R.DS_OK
+        hdr = pk.arrays()["header"]
+        assert hdr[14] == want, (wl.name, hdr[14], pk.meta.prefill_sms)
+        assert list(hdr[[4, 5, 11, 12, 13]]) == [0, 0, 0, 0, 0]
