@@ -51,11 +51,11 @@ SINGLE_THREAD_ORACLE = ("tiny_gqa_d64", "decode256_mha_d128", "splitfuse2048_gqa
 # removed) still matches the capture.
 NCU_TRAFFIC = {
     # decode_split_kernel on the first 64 sequences of the decode-only batch:
-    # 2.290063 GB read + 6.02 MB written for 2.2576 GB algorithmic (x1.0171);
+    # 2.290075 GB read + 6.03 MB written for 2.2576 GB algorithmic (x1.0171);
     # scaled to the full batch by its algorithmic bytes (the KV read dominates
     # and grows in proportion).
-    "decode256_mha_d128": {"bytes": 9.3776e9, "files": ["decode.cu", "common.cuh", "tc.cuh"],
-                           "src": "69acc4e8a58215d6"},
+    "decode256_mha_d128": {"bytes": 9.3774e9, "files": ["decode.cu", "common.cuh", "tc.cuh"],
+                           "src": "eb2b8af3571b7705"},
     # prefill_tc_kernel on the whole chunked-prefill workload (< 1 GB on the
     # device, captured at full size): 459.60 MB read + 226.74 MB written for
     # 637.5 MB algorithmic (x1.077).
