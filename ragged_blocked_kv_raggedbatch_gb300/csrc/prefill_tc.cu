@@ -98,11 +98,16 @@ constexpr int AQ = 4;
 enum {
   B_QREADY = 0, B_KFULL = 2, B_VFULL = 4, B_KEMPTY = 6, B_SFULL = 8, B_PFULL = 10,
   B_ODONE = 14, B_ODONE0 = 16, B_VLAST = 18, B_DONE = 19, B_VEMPTY = 20, B_AFULL = 22,
-  B_AEMPTY = B_AFULL + AQ, B_COUNT = B_AEMPTY + AQ
+  B_AEMPTY = B_AFULL + AQ, B_QRAW = B_AEMPTY + AQ, B_OSTG = B_QRAW + 2, B_OFREE = B_OSTG + 2,
+  B_COUNT = B_OFREE + 2
 };
 // arrivals that free an atom slot: the MMA warp, 8 softmax warps
 constexpr int AEMPTY_ARRIVALS = 9;
-static_assert(8 * B_COUNT + 4 + 4 * AQ <= 512, "barriers, tensor-memory slot and atom ring fit the reserved bytes");
+// an atom ring slot: index, valid flag, then the atom's fields as the
+// producer decoded them (seq, j0, ntok, kv_len, c, seen, first token, block
+// table offset), so the other roles read no metadata from global memory
+constexpr int AW = 10;
+static_assert(8 * B_COUNT + 4 + 4 * AW * AQ <= 512, "barriers, tensor-memory slot and atom ring fit the reserved bytes");
 
 template <bool BF16, bool HALF, int D, int G, bool FUSED>
 __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
@@ -202,6 +207,11 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
       mbar_init(&bar[B_AEMPTY + q], AEMPTY_ARRIVALS);
     }
     mbar_init(&bar[B_DONE], 256);
+    for (int s = 0; s < 2; ++s) {  // the 4 softmax warps of a tile
+      mbar_init(&bar[B_QRAW + s], 4);
+      mbar_init(&bar[B_OSTG + s], 4);
+      mbar_init(&bar[B_OFREE + s], 4);
+    }
     fence_barrier_init();
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -224,16 +234,6 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
   // atoms span 32 to 24,872 keys; a scheduler warp filling the ring ahead let
   // one CTA take several of the longest atoms at once.  next_atom returns -1
   // when the atoms are exhausted or a wait ran out (then ok = false).
-  auto next_atom = [&](uint32_t& i, bool& ok) -> int {
-    const int q = i % AQ;
-    const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&bar[B_AFULL + q], (i / AQ) & 1));
-    const int k = got ? aring[q] : -1;
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&bar[B_AEMPTY + q]);
-    ++i;
-    if (!got) ok = false;
-    return k;
-  };
   struct Atom {
     int seq, j0, ntok, kv_len, c, s_seen, tok0, n_kv;
     bool has_b;
@@ -272,6 +272,30 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
     }
     return true;
   };
+  // The next atom from the ring (AQ slots the producer fills in order): its
+  // index (-1 when the atoms are exhausted or a wait ran out, then ok =
+  // false), whether it is well formed, and its fields.
+  auto next_atom = [&](uint32_t& i, bool& ok, Atom& at, bool& valid) -> int {
+    const int q = i % AQ;
+    const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&bar[B_AFULL + q], (i / AQ) & 1));
+    int k = -1;
+    valid = false;
+    if (got) {
+      const int* sl = aring + q * AW;
+      k = sl[0];
+      valid = sl[1] != 0;
+      at.seq = sl[2]; at.j0 = sl[3]; at.ntok = sl[4]; at.kv_len = sl[5];
+      at.c = sl[6]; at.s_seen = sl[7]; at.tok0 = sl[8];
+      at.btab = block_table + sl[9];
+      at.has_b = at.ntok > T;
+      at.n_kv = (at.kv_len + C::KEYS - 1) / C::KEYS;
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&bar[B_AEMPTY + q]);
+    ++i;
+    if (!got) ok = false;
+    return k;
+  };
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(DSR_PF_REG_LOW) : "memory");
@@ -297,13 +321,21 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
         if (lane == 0) k = atomicAdd(&hdr[HDR_PRE_NEXT], 1);
         k = __shfl_sync(0xffffffffu, k, 0);
         if (k >= n_atoms) k = -1;
+        Atom at;
+        const bool valid = k >= 0 && load_atom(k, at);
         if (lane == 0) {
-          aring[q] = k;
+          int* sl = aring + q * AW;
+          sl[0] = k;
+          sl[1] = valid ? 1 : 0;
+          if (valid) {
+            sl[2] = at.seq; sl[3] = at.j0; sl[4] = at.ntok; sl[5] = at.kv_len;
+            sl[6] = at.c; sl[7] = at.s_seen; sl[8] = at.tok0;
+            sl[9] = (int)(at.btab - block_table);
+          }
           tc::mbar_arrive(&bar[B_AFULL + q]);
         }
         if (k < 0) break;
-        Atom at;
-        if (!load_atom(k, at)) continue;
+        if (!valid) continue;
         for (int t = 0; t < at.n_kv; ++t, ++ring) {
           const int st = ring & 1;
           const uint32_t empty_par = ((ring >> 1) - 1) & 1;
@@ -423,10 +455,11 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
         uint32_t ring = 0, qn[2] = {0, 0}, stp[2] = {0, 0};
         bool ok = true;
         for (uint32_t ai = 0; ok;) {
-          const int k = next_atom(ai, ok);
-          if (k < 0) break;
           Atom at;
-          if (!load_atom(k, at)) continue;
+          bool av;
+          const int k = next_atom(ai, ok, at, av);
+          if (k < 0) break;
+          if (!av) continue;
           ok = wait(B_QREADY + 0, qn[0] & 1) && wait(B_KFULL + (ring & 1), (ring >> 1) & 1);
           ++qn[0];
           if (!ok) break;
@@ -483,40 +516,70 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
     const uint32_t col_s = C::COL_S0 + 128 * x;
     const uint32_t col_o = C::COL_O0 + D * x;
     const float sc = a.scale_log2;
-    uint32_t stp = 0;  // KV steps of tile x done by this CTA
+    uint32_t stp = 0;   // KV steps of tile x done by this CTA
+    uint32_t qraw = 0;  // Q tiles this tile's warps copied
+    uint32_t ostg = 0;  // outputs this tile's warps staged and wrote
     bool ok = true;
     for (uint32_t ai = 0; ok;) {
-      const int k = next_atom(ai, ok);
-      if (k < 0) break;
       Atom at;
-      if (!load_atom(k, at)) continue;
+      bool av;
+      const int k = next_atom(ai, ok, at, av);
+      if (k < 0) break;
+      if (!av) continue;
       if (x == 1 && !at.has_b) continue;
       const int jt = x * T + r / G;             // token of this row inside the atom
       const bool valid = jt < at.ntok;
-      const int head = at.c * G + r % G;
       const int pos = at.s_seen + at.j0 + min(jt, at.ntok - 1);
 
-      // Q row: rotate on load, round to the storage type, 128-byte swizzle.
+      // Q tile: the tile's 4 warps copy its 128 rows (row r = token r / G,
+      // head r % G of KV group c) into 128-byte-swizzled shared memory with
+      // coalesced 16-byte loads (the G heads of a token are contiguous), meet
+      // at a bounded barrier, then each thread rotates its own row in place
+      // (fp32, same rule as the append).  One thread loading its own row took
+      // ~9000 cycles between two atoms: 32 rows per warp instruction.
       {
         uint8_t* qt = sQ + x * C::QTILE;
-        const float4* cs4 = reinterpret_cast<const float4*>(a.rope) + (int64_t)pos * (D / 4);
-        const uint16_t* src =
-            qkv + (int64_t)(at.tok0 + min(jt, at.ntok - 1)) * ((a.Hq + 2 * a.Hkv) * D) + head * D;
+        const int64_t rs = (int64_t)(a.Hq + 2 * a.Hkv) * D;  // qkv row stride
+        constexpr int CPR = D / 8;                           // 16-byte chunks per row
+        constexpr int PER = 128 * CPR / 128;                 // chunks per thread
+        const int tt = 32 * (warp & 3) + lane;               // 0..127 within the tile
+        uint4 raw[PER];
 #pragma unroll
-        for (int cc = 0; cc < D / 16; ++cc) {
-          const int ch0 = HALF ? cc : 2 * cc;
-          const int ch1 = HALF ? D / 16 + cc : 2 * cc + 1;
-          uint4 x0 = make_uint4(0, 0, 0, 0), x1 = make_uint4(0, 0, 0, 0);
-          if (valid) {
-            x0 = ld_nc_v4(src + 8 * ch0);
-            x1 = ld_nc_v4(src + 8 * ch1);
+        for (int k2 = 0; k2 < PER; ++k2) {
+          const int i = tt + 128 * k2, row = i / CPR, cc = i % CPR;
+          const int tj = x * T + row / G;
+          raw[k2] = make_uint4(0, 0, 0, 0);
+          if (tj < at.ntok)
+            raw[k2] = ld_nc_v4(qkv + (int64_t)(at.tok0 + tj) * rs + (at.c * G + row % G) * D + 8 * cc);
+        }
+#pragma unroll
+        for (int k2 = 0; k2 < PER; ++k2) {
+          const int i = tt + 128 * k2, row = i / CPR, cc = i % CPR;
+          *reinterpret_cast<uint4*>(qt + (cc / 8) * C::QHALF + row * 128 + (((cc % 8) ^ (row & 7)) << 4)) = raw[k2];
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[B_QRAW + x]);
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bar[B_QRAW + x], qraw & 1))) {
+          ok = false;
+          break;
+        }
+        ++qraw;
+        if (valid) {
+          const float4* cs4 = reinterpret_cast<const float4*>(a.rope) + (int64_t)pos * (D / 4);
+#pragma unroll
+          for (int cc = 0; cc < D / 16; ++cc) {
+            const int ch0 = HALF ? cc : 2 * cc;
+            const int ch1 = HALF ? D / 16 + cc : 2 * cc + 1;
+            uint4* p0 = reinterpret_cast<uint4*>(qt + (ch0 / 8) * C::QHALF + r * 128 + (((ch0 % 8) ^ (r & 7)) << 4));
+            uint4* p1 = reinterpret_cast<uint4*>(qt + (ch1 / 8) * C::QHALF + r * 128 + (((ch1 % 8) ^ (r & 7)) << 4));
+            uint4 x0 = *p0, x1 = *p1;
             float4 cs[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) cs[q] = __ldg(cs4 + 4 * cc + q);
             rotate16<BF16, HALF>(x0, x1, cs);
+            *p0 = x0;
+            *p1 = x1;
           }
-          *reinterpret_cast<uint4*>(qt + (ch0 / 8) * C::QHALF + r * 128 + (((ch0 % 8) ^ (r & 7)) << 4)) = x0;
-          *reinterpret_cast<uint4*>(qt + (ch1 / 8) * C::QHALF + r * 128 + (((ch1 % 8) ^ (r & 7)) << 4)) = x1;
         }
         tc::fence_proxy_async();
         tc::mbar_arrive(&bar[B_QREADY + x]);
@@ -610,26 +673,53 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(
         l = l * alpha + (s0 + s1);
       }
       if (!ok) break;
-      // epilogue: the atom's last P*V, then O / l -> out
+      // epilogue: the atom's last P*V, then O / l -> out.  Each thread
+      // stages its row in the tile's Q buffer (its last QK is done), the 4
+      // warps meet, and they write the rows out with coalesced 16-byte
+      // stores (a thread storing its own row: 32 rows per warp instruction).
       if (!mbar_wait_bounded(&bar[B_ODONE + x], (stp - 1) & 1)) { ok = false; break; }
       tc::fence_after();
-      const float inv = 1.f / l;
-      uint16_t* dst = out + (int64_t)(at.tok0 + jt) * a.Hq * D + head * D;
+      {
+        const float inv = 1.f / l;
+        uint8_t* qt = sQ + x * C::QTILE;
+        uint32_t v[D];
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t v[32];
-        tc::tmem_ld32(lane_addr + col_o + 32 * ch, v);
+        for (int ch = 0; ch < D / 32; ++ch) tc::tmem_ld32(lane_addr + col_o + 32 * ch, v + 32 * ch);
         tc::tmem_wait_ld();
-        if (valid) {
-          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = Stor<BF16>::pack(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+        for (int cc = 0; cc < D / 8; ++cc) {
+          uint32_t pk[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(dst + 32 * ch + 8 * q) =
-                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int e = 0; e < 4; ++e)
+            pk[e] = Stor<BF16>::pack(__uint_as_float(v[8 * cc + 2 * e]) * inv,
+                                     __uint_as_float(v[8 * cc + 2 * e + 1]) * inv);
+          *reinterpret_cast<uint4*>(qt + (cc / 8) * C::QHALF + r * 128 + (((cc % 8) ^ (r & 7)) << 4)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[B_OSTG + x]);
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bar[B_OSTG + x], ostg & 1))) {
+          ok = false;
+          break;
+        }
+        constexpr int CPR = D / 8;            // 16-byte chunks per row
+        const int tt = 32 * (warp & 3) + lane;
+#pragma unroll
+        for (int k2 = 0; k2 < CPR; ++k2) {
+          const int i = tt + 128 * k2, row = i / CPR, cc = i % CPR;
+          const int tj = x * T + row / G;
+          if (tj < at.ntok)
+            *reinterpret_cast<uint4*>(out + (int64_t)(at.tok0 + tj) * a.Hq * D + (at.c * G + row % G) * D + 8 * cc) =
+                *reinterpret_cast<const uint4*>(qt + (cc / 8) * C::QHALF + row * 128 + (((cc % 8) ^ (row & 7)) << 4));
+        }
+        // the staging buffer is the next atom's Q buffer: every warp has read it first
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar[B_OFREE + x]);
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bar[B_OFREE + x], ostg & 1))) {
+          ok = false;
+          break;
+        }
+        ++ostg;
       }
     }
     if (!ok) set_dev_error(a.header, DS_DEVERR_WORKLIST);
