@@ -57,10 +57,10 @@ NCU_TRAFFIC = {
     "decode256_mha_d128": {"bytes": 9.3774e9, "files": ["decode.cu", "common.cuh", "tc.cuh"],
                            "src": "eb2b8af3571b7705"},
     # prefill_tc_kernel on the whole chunked-prefill workload (< 1 GB on the
-    # device, captured at full size): 459.60 MB read + 226.74 MB written for
-    # 637.5 MB algorithmic (x1.077).
-    "chunked_prefill_2x8192": {"bytes": 6.86337e8, "files": ["prefill_tc.cu", "common.cuh", "tc.cuh"],
-                               "src": "7aee36208be0d9b6"},
+    # device, captured at full size): 461.19 MB read + 231.07 MB written for
+    # 637.5 MB algorithmic (x1.086).
+    "chunked_prefill_2x8192": {"bytes": 6.92260e8, "files": ["prefill_tc.cu", "common.cuh", "tc.cuh"],
+                               "src": "60e9f76d72cc4bee"},
 }
 
 
