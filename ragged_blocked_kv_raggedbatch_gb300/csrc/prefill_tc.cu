@@ -16,8 +16,9 @@
 // first warpgroup gives registers back (setmaxnreg 96) and the two softmax
 // warpgroups take them (setmaxnreg 200): 128*96 + 2*128*200 <= 384*168):
 //   warp 0      takes the atoms (longest first, from a counter in the batch
-//               header, one as the previous one's last tile is issued) and
-//               hands them to the others; TMA producer: K and V tiles into
+//               header, one as the previous one's last tile is issued),
+//               decodes them and hands them to the others through a ring in
+//               shared memory; TMA producer: K and V tiles into
 //               2-stage rings whose slots are
 //               freed separately (K after the last QK MMA that reads it, V after
 //               the last PV MMA), so each K tile is requested about a step and a
@@ -34,12 +35,15 @@
 //               so one tile's softmax overlaps the other tile's MMAs.
 //   warps 2-3   no work (they only return their registers)
 //   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: one thread per
-//               row (tensor-memory lane = row); builds its Q row (rotated on
-//               load, fp32, same rule as the append) in 128-byte-swizzled shared
-//               memory; per KV tile: masked row max, conditional rescale of O
-//               (only when the max grows by more than 2^8: the reference max may
-//               lag, the final O / l is exact), P = exp2(S - m) written back over
-//               S as packed 16-bit pairs; epilogue O / l -> out.
+//               row (tensor-memory lane = row).  Per atom the tile's 4 warps
+//               copy its Q rows into 128-byte-swizzled shared memory with
+//               coalesced loads, then each thread rotates its own row in place
+//               (fp32, same rule as the append); per KV tile: masked row max,
+//               conditional rescale of O (only when the max grows by more than
+//               2^8: the reference max may lag, the final O / l is exact),
+//               P = exp2(S - m) written back over S as packed 16-bit pairs;
+//               epilogue: O / l staged in the tile's Q buffer, written out with
+//               coalesced stores.
 // Tensor memory: S_A [0,128) S_B [128,256) O_A [256,256+D) O_B [256+D,256+2D).
 // Every mbarrier wait is bounded: on timeout the CTA records an error and stops.
 #include <algorithm>
