@@ -159,8 +159,10 @@ typedef struct ds_ragged_meta {
     size_t used_bytes;    /* bytes uploaded                                  */
     /* DEVICE pointers into device_buf (int32 unless noted):
      *   header[16]        word 0: device error bits, 1: S, 2: N, 3: blocks;
- *                     the rest are the work-list counts and the kernels'
- *                     own counters (internal; zero after each upload)
+     *                     the rest are the work-list counts, the prefill
+     *                     grid size and atom order the pack chose, and the
+     *                     kernels' own counters (internal; the counters are
+     *                     zero after each upload)
      *   cu_seqlens[S+1]   exclusive prefix sum of new_tokens
      *   seq_seen[S], seq_new[S]
      *   blk_off[S+1]      exclusive prefix sum of ceil((seen+new)/block_size)
